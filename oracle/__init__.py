@@ -1,0 +1,152 @@
+"""fp64 CPU oracle for exact softmax attention -- TEST INFRASTRUCTURE ONLY.
+
+Only the test suite, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU
+baseline / reference leg may import this package.  The product library
+(``exact_io_aware_06_gb300``) never imports, links or runs it, and the two
+share no code.
+
+Functions (numpy in, numpy out; every array is promoted to float64):
+
+* ``attn_fwd(q, k, v, scale, causal)`` -- standard attention written out
+  (S = scale QK^T, stable row softmax, O = PV, lse = m + ln l), following the
+  "FlashAttention-1" page, 10.2.1, and the Python demo's ``softmax_attention``
+  on the "Flash Attention V1/V2/V3" page.
+* ``attn_fwd_rows(q, k, v, rows, scale, causal)`` -- the same for selected
+  rows of one head (rows are independent in the forward).
+* ``attn_fwd_tiled(q, k, v, Br, Bc, scale, causal)`` -- online softmax over
+  blocks ("Flash Attention V1/V2/V3" page, Python demo; "5.4 FlashAttention"
+  page, listing 3-1), used only for block-size invariance checks.
+* ``attn_bwd(q, k, v, do, scale, causal)`` -- analytic backward
+  ("FlashAttention-1" page, 10.2.4): dV = P^T dO, dP = dO V^T,
+  dS = P o (dP - delta), delta_i = dO_i . O_i, dQ = scale dS K,
+  dK = scale dS^T Q.
+* ``e4m3_decode(codes, descale)`` / ``e4m3_encode(x)`` -- OCP FP8 E4M3.
+
+Tensors are ``[..., N, d]``; leading dimensions are flattened into heads.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_LIB = None
+
+_dp = ctypes.POINTER(ctypes.c_double)
+_lp = ctypes.POINTER(ctypes.c_long)
+_u8p = ctypes.POINTER(ctypes.c_uint8)
+
+
+def lib():
+    global _LIB
+    if _LIB is None:
+        path = _build.LIB
+        if not os.path.exists(path) or not _build.up_to_date():
+            _build.build()
+        L = ctypes.CDLL(path)
+        L.oracle_fwd.argtypes = [_dp, _dp, _dp, ctypes.c_long, ctypes.c_long, ctypes.c_long,
+                                 ctypes.c_double, ctypes.c_int, _dp, _dp, ctypes.c_int]
+        L.oracle_fwd_rows.argtypes = [_dp, _dp, _dp, ctypes.c_long, ctypes.c_long,
+                                      ctypes.c_double, ctypes.c_int, _lp, ctypes.c_long, _dp, _dp,
+                                      ctypes.c_int]
+        L.oracle_fwd_tiled.argtypes = [_dp, _dp, _dp, ctypes.c_long, ctypes.c_long, ctypes.c_long,
+                                       ctypes.c_double, ctypes.c_int, ctypes.c_long,
+                                       ctypes.c_long, _dp, _dp]
+        L.oracle_bwd.argtypes = [_dp, _dp, _dp, _dp, ctypes.c_long, ctypes.c_long, ctypes.c_long,
+                                 ctypes.c_double, ctypes.c_int, _dp, _dp, _dp, ctypes.c_int]
+        L.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+        L.oracle_e4m3_to_f64.restype = ctypes.c_double
+        L.oracle_f64_to_e4m3.argtypes = [ctypes.c_double]
+        L.oracle_f64_to_e4m3.restype = ctypes.c_uint8
+        L.oracle_e4m3_decode.argtypes = [_u8p, ctypes.c_long, ctypes.c_double, _dp]
+        L.oracle_e4m3_encode.argtypes = [_dp, ctypes.c_long, _u8p]
+        L.oracle_max_threads.restype = ctypes.c_int
+        _LIB = L
+    return _LIB
+
+
+def max_threads():
+    return int(lib().oracle_max_threads())
+
+
+def _f64(x):
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a, t=_dp):
+    return a.ctypes.data_as(t)
+
+
+def _heads(q, k, v):
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    if q.shape != k.shape or q.shape != v.shape or q.ndim < 2:
+        raise ValueError("q, k, v must share one shape [..., N, d]")
+    N, d = q.shape[-2], q.shape[-1]
+    BH = int(np.prod(q.shape[:-2])) if q.ndim > 2 else 1
+    return q, k, v, BH, N, d
+
+
+def attn_fwd(q, k, v, scale, causal=False, nthreads=0):
+    """Return (O, lse): O has q's shape, lse has q.shape[:-1]."""
+    q, k, v, BH, N, d = _heads(q, k, v)
+    o = np.empty_like(q)
+    lse = np.empty(q.shape[:-1], dtype=np.float64)
+    lib().oracle_fwd(_ptr(q), _ptr(k), _ptr(v), BH, N, d, float(scale), int(bool(causal)),
+                     _ptr(o), _ptr(lse), int(nthreads))
+    return o, lse
+
+
+def attn_fwd_rows(q, k, v, rows, scale, causal=False, nthreads=0):
+    """One head ([N, d] each); rows: query indices.  Returns (O[rows], lse[rows])."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    if q.ndim != 2:
+        raise ValueError("attn_fwd_rows takes one head: [N, d]")
+    N, d = q.shape
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64)).astype(np.int_)
+    if rows.size and (rows.min() < 0 or rows.max() >= N):
+        raise ValueError("row index out of range")
+    o = np.empty((rows.size, d), dtype=np.float64)
+    lse = np.empty(rows.size, dtype=np.float64)
+    lib().oracle_fwd_rows(_ptr(q), _ptr(k), _ptr(v), N, d, float(scale), int(bool(causal)),
+                          _ptr(rows, _lp), rows.size, _ptr(o), _ptr(lse), int(nthreads))
+    return o, lse
+
+
+def attn_fwd_tiled(q, k, v, Br, Bc, scale, causal=False):
+    q, k, v, BH, N, d = _heads(q, k, v)
+    if Br < 1 or Bc < 1:
+        raise ValueError("block sizes must be >= 1")
+    o = np.empty_like(q)
+    lse = np.empty(q.shape[:-1], dtype=np.float64)
+    lib().oracle_fwd_tiled(_ptr(q), _ptr(k), _ptr(v), BH, N, d, float(scale),
+                           int(bool(causal)), int(Br), int(Bc), _ptr(o), _ptr(lse))
+    return o, lse
+
+
+def attn_bwd(q, k, v, do, scale, causal=False, nthreads=0):
+    """Return (dQ, dK, dV) of L = <dO, O(q, k, v)>."""
+    q, k, v, BH, N, d = _heads(q, k, v)
+    do = _f64(do)
+    if do.shape != q.shape:
+        raise ValueError("dO must have q's shape")
+    dq, dk, dv = np.empty_like(q), np.empty_like(q), np.empty_like(q)
+    lib().oracle_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(do), BH, N, d, float(scale),
+                     int(bool(causal)), _ptr(dq), _ptr(dk), _ptr(dv), int(nthreads))
+    return dq, dk, dv
+
+
+def e4m3_decode(codes, descale=1.0):
+    """uint8 E4M3 codes -> float64 values times descale."""
+    c = np.ascontiguousarray(np.asarray(codes, dtype=np.uint8))
+    out = np.empty(c.shape, dtype=np.float64)
+    lib().oracle_e4m3_decode(_ptr(c, _u8p), c.size, float(descale), _ptr(out))
+    return out
+
+
+def e4m3_encode(x):
+    """float64 values -> uint8 E4M3 codes (round to nearest even, saturate at 448)."""
+    x = _f64(x)
+    out = np.empty(x.shape, dtype=np.uint8)
+    lib().oracle_e4m3_encode(_ptr(x), x.size, _ptr(out, _u8p))
+    return out
