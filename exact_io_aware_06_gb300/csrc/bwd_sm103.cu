@@ -1,0 +1,546 @@
+// bwd_sm103.cu -- attention backward by recomputation on the sm_103a tensor core.
+//
+// The "FlashAttention-1" page (10.2.4) keeps only O and the softmax statistics
+// from the forward and rebuilds P block by block:
+//     P_ij = exp(S_ij - lse_i),  dV = P^T dO,  dP = dO V^T,
+//     delta_i = dO_i . O_i,      dS = P o (dP - delta),
+//     dQ = scale dS K,           dK = scale dS^T Q.
+// (The page's rowsum(dP o P) form of the softmax backward is the same delta:
+// rowsum(dP o P)_i = sum_j P_ij dO_i . V_j = dO_i . O_i.)
+//
+// Three kernels on one stream:
+//   1. bwd_prep      delta_i (fp32), lse_i * log2(e) copied into a padded
+//                    workspace row, and the fp32 dQ accumulator zeroed.
+//   2. bwd_main      one CTA per (head, 128-key block j), looping over all
+//                    128-row query blocks i; dK_j and dV_j accumulate in TMEM
+//                    for the whole loop, dQ_i partials go to the fp32
+//                    accumulator with vector atomics.
+//   3. bwd_dq_convert  dQ = bf16(scale * accumulator).
+//
+// bwd_main layout (d = 64):
+//   warp 0      TMA producer: K_j, V_j once; Q_i, dO_i, lse_i, delta_i in a 2-stage ring
+//   warp 1      MMA issuer + TMEM owner
+//   warps 4-7   "P/dS" warpgroup: thread = key row of the block
+//   warps 8-11  "dQ" warpgroup: drains dQ_i from TMEM into the accumulator
+//   TMEM: S^T 0-127 (P^T bf16 over 0-63), dP^T 128-255 (dS^T bf16 over 128-191),
+//         dV 256-319, dK 320-383, dQ double buffer 384-447 / 448-511.
+//   MMAs per query block i (M = 128 keys or queries):
+//     S^T  = K_j Q_i^T        (SS, both K-major)
+//     dP^T = V_j dO_i^T       (SS, both K-major)
+//     dV  += P^T dO_i         (TS, dO_i MN-major)
+//     dK  += dS^T Q_i         (TS, Q_i MN-major)
+//     dQ_i = dS K_j           (SS, dS from shared memory MN-major, K_j MN-major)
+#include <cmath>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "tma_host.h"
+
+namespace fa {
+namespace {
+
+constexpr int kD = 64;
+constexpr int kBlk = 128;            // keys per CTA, queries per inner step
+constexpr int kThreads = 384;
+constexpr int kTile = kBlk * kD * 2;  // 16 KB bf16 tile (one 128-byte swizzle column)
+constexpr float kLog2e = 1.4426950408889634f;
+
+// shared memory map (offsets from a 1 KB aligned base)
+constexpr int kOffK = 0;
+constexpr int kOffV = kOffK + kTile;
+constexpr int kOffQ = kOffV + kTile;             // 2 stages
+constexpr int kOffDO = kOffQ + 2 * kTile;        // 2 stages
+constexpr int kOffDS = kOffDO + 2 * kTile;       // 2 buffers x 32 KB (two 64-query columns)
+constexpr int kDSBytes = kBlk * kBlk * 2;
+constexpr int kOffL = kOffDS + 2 * kDSBytes;     // 2 stages x 512 B
+constexpr int kOffDelta = kOffL + 2 * kBlk * 4;  // 2 stages x 512 B
+constexpr int kSmemBytes = kOffDelta + 2 * kBlk * 4;
+constexpr int kSmemAlloc = kSmemBytes + 1024;
+
+constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 320, kColDQ = 384;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kIdescSS = idesc_bf16(128, 128, false, false);  // S^T, dP^T
+constexpr uint32_t kIdescTS = idesc_bf16(128, kD, false, true);    // dV, dK
+constexpr uint32_t kIdescDQ = idesc_bf16(128, kD, true, true);     // dQ (A MN-major)
+
+struct BwdArgs {
+    const float* ws_delta;  // [BH][Np]
+    const float* ws_lse2;   // [BH][Np]
+    float* dq_acc;          // [BH][Np][d]
+    void* dk;
+    void* dv;
+    int N, Np, n_kv;
+    float c_log2;           // scale * log2(e)
+    float scale;
+    DevCtl ctl;
+};
+
+struct Bars {
+    uint64_t kv_full;
+    uint64_t q_full[2], q_empty[2];
+    uint64_t s_full, dp_full, p_full, ds_full;
+    uint64_t ds_empty[2];
+    uint64_t dq_full[2], dq_free[2];
+    uint64_t all_done;
+    uint64_t drain;
+};
+
+__device__ __forceinline__ void record_timeout(const DevCtl& ctl, volatile int* abort_flag) {
+    *abort_flag = 1;
+    atomicCAS(ctl.status, kDevOk, kDevTimeout);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const BwdArgs args) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) Bars bars;
+    __shared__ uint32_t tmem_slot;
+    __shared__ volatile int abort_flag;
+
+    const uint32_t sb = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    uint8_t* const sb_ptr = smem_raw + (sb - smem_u32(smem_raw));
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int bh = blockIdx.x / args.n_kv;
+    const int kvb = blockIdx.x % args.n_kv;
+    const int N = args.N, Np = args.Np;
+    const int n_q = Np / kBlk;
+    const uint64_t lim = args.ctl.wait_ns;
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(smem_u32(&bars.kv_full), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(smem_u32(&bars.q_full[s]), 1);
+            mbar_init(smem_u32(&bars.q_empty[s]), 1);
+            mbar_init(smem_u32(&bars.ds_empty[s]), 1);
+            mbar_init(smem_u32(&bars.dq_full[s]), 1);
+            mbar_init(smem_u32(&bars.dq_free[s]), 128);
+        }
+        mbar_init(smem_u32(&bars.s_full), 1);
+        mbar_init(smem_u32(&bars.dp_full), 1);
+        mbar_init(smem_u32(&bars.p_full), 128);
+        mbar_init(smem_u32(&bars.ds_full), 128);
+        mbar_init(smem_u32(&bars.all_done), 1);
+        mbar_init(smem_u32(&bars.drain), 1);
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        tma_prefetch_desc(&tm_do);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+
+    if (warp == 0) {
+        // ================================================================ producer
+        if (lane == 0) {
+            const uint32_t kvf = smem_u32(&bars.kv_full);
+            mbar_arrive_expect_tx(kvf, 2 * kTile);
+            tma_load_3d(sb + kOffK, &tm_k, kvf, 0, kvb * kBlk, bh);
+            tma_load_3d(sb + kOffV, &tm_v, kvf, 0, kvb * kBlk, bh);
+            int issued = 0;
+            bool ok = true;
+            for (int i = 0; i < n_q; ++i) {
+                const int s = i & 1;
+                if (i >= 2 && !mbar_wait(smem_u32(&bars.q_empty[s]), ((i >> 1) & 1) ^ 1, lim, &abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t qf = smem_u32(&bars.q_full[s]);
+                mbar_arrive_expect_tx(qf, 2 * kTile + 2 * kBlk * 4);
+                tma_load_3d(sb + kOffQ + s * kTile, &tm_q, qf, 0, i * kBlk, bh);
+                tma_load_3d(sb + kOffDO + s * kTile, &tm_do, qf, 0, i * kBlk, bh);
+                const size_t row = static_cast<size_t>(bh) * Np + static_cast<size_t>(i) * kBlk;
+                bulk_load(sb + kOffL + s * kBlk * 4, args.ws_lse2 + row, kBlk * 4, qf);
+                bulk_load(sb + kOffDelta + s * kBlk * 4, args.ws_delta + row, kBlk * 4, qf);
+                issued = i + 1;
+            }
+            if (!ok) record_timeout(args.ctl, &abort_flag);
+            const volatile int never = 0;
+            mbar_wait(kvf, 0, kDrainWaitNs, &never);
+            for (int i = max(0, issued - 2); i < issued; ++i)
+                mbar_wait(smem_u32(&bars.q_full[i & 1]), (i >> 1) & 1, kDrainWaitNs, &never);
+        }
+    } else if (warp == 1) {
+        // ================================================================ MMA issuer
+        if (lane == 0) {
+            const uint32_t sK = sb + kOffK, sV = sb + kOffV;
+            bool ok = mbar_wait(smem_u32(&bars.kv_full), 0, lim, &abort_flag);
+            // S^T = K_j Q_i^T and dP^T = V_j dO_i^T for query block i (stage s)
+            auto issue_s_dp = [&](int s) {
+                const uint32_t sQ = sb + kOffQ + s * kTile, sDO = sb + kOffDO + s * kTile;
+#pragma unroll
+                for (int kk = 0; kk < kD / 16; ++kk)
+                    mma_bf16_ss(tmem + kColS, sdesc_sw128(sK + 32 * kk, 16, 1024),
+                                sdesc_sw128(sQ + 32 * kk, 16, 1024), kIdescSS, kk > 0);
+                mma_commit(smem_u32(&bars.s_full));
+#pragma unroll
+                for (int kk = 0; kk < kD / 16; ++kk)
+                    mma_bf16_ss(tmem + kColDP, sdesc_sw128(sV + 32 * kk, 16, 1024),
+                                sdesc_sw128(sDO + 32 * kk, 16, 1024), kIdescSS, kk > 0);
+                mma_commit(smem_u32(&bars.dp_full));
+            };
+            if (ok) ok = mbar_wait(smem_u32(&bars.q_full[0]), 0, lim, &abort_flag);
+            if (ok) {
+                tc_fence_after();
+                issue_s_dp(0);
+            }
+            for (int i = 0; i < n_q && ok; ++i) {
+                const int s = i & 1;
+                const uint32_t sQ = sb + kOffQ + s * kTile, sDO = sb + kOffDO + s * kTile;
+                // dV += P^T dO_i
+                ok = mbar_wait(smem_u32(&bars.p_full), i & 1, lim, &abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < kBlk / 16; ++kk)
+                    mma_bf16_ts(tmem + kColDV, tmem + kColS + 8 * kk,
+                                sdesc_sw128(sDO + 2048 * kk, 16384, 1024), kIdescTS, (i > 0) || (kk > 0));
+                // dK += dS^T Q_i
+                ok = mbar_wait(smem_u32(&bars.ds_full), i & 1, lim, &abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < kBlk / 16; ++kk)
+                    mma_bf16_ts(tmem + kColDK, tmem + kColDP + 8 * kk,
+                                sdesc_sw128(sQ + 2048 * kk, 16384, 1024), kIdescTS, (i > 0) || (kk > 0));
+                mma_commit(smem_u32(&bars.q_empty[s]));  // Q_i, dO_i, lse_i, delta_i consumed
+                // next block's S^T and dP^T overlap with this block's dQ
+                if (i + 1 < n_q) {
+                    ok = mbar_wait(smem_u32(&bars.q_full[s ^ 1]), ((i + 1) >> 1) & 1, lim, &abort_flag);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_s_dp(s ^ 1);
+                }
+                // dQ_i = dS_i K_j into TMEM buffer s
+                if (i >= 2) {
+                    ok = mbar_wait(smem_u32(&bars.dq_free[s]), ((i >> 1) & 1) ^ 1, lim, &abort_flag);
+                    if (!ok) break;
+                    tc_fence_after();
+                }
+                const uint32_t sDS = sb + kOffDS + s * kDSBytes;
+#pragma unroll
+                for (int kk = 0; kk < kBlk / 16; ++kk)
+                    mma_bf16_ss(tmem + kColDQ + 64 * s, sdesc_sw128(sDS + 2048 * kk, 16384, 1024),
+                                sdesc_sw128(sK + 2048 * kk, 16384, 1024), kIdescDQ, kk > 0);
+                mma_commit(smem_u32(&bars.dq_full[s]));
+                mma_commit(smem_u32(&bars.ds_empty[s]));
+            }
+            if (ok) mma_commit(smem_u32(&bars.all_done));
+            if (!ok) record_timeout(args.ctl, &abort_flag);
+            mma_commit(smem_u32(&bars.drain));
+            const volatile int never = 0;
+            mbar_wait(smem_u32(&bars.drain), 0, kDrainWaitNs, &never);
+        }
+    } else if (warp >= 4 && warp < 8) {
+        // ================================================================ P / dS warpgroup
+        const int wq = warp % 4;
+        const int key_in_blk = wq * 32 + lane;
+        const uint32_t lb = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+        const float c = args.c_log2;
+        bool ok = true;
+        for (int i = 0; i < n_q; ++i) {
+            const int s = i & 1;
+            ok = mbar_wait(smem_u32(&bars.q_full[s]), (i >> 1) & 1, lim, &abort_flag);
+            if (ok) ok = mbar_wait(smem_u32(&bars.s_full), i & 1, lim, &abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            const float4* L4 = reinterpret_cast<const float4*>(sb_ptr + kOffL + s * kBlk * 4);
+            const float4* D4 = reinterpret_cast<const float4*>(sb_ptr + kOffDelta + s * kBlk * 4);
+            uint32_t pk[64];  // P^T row, bf16 pairs
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                uint32_t r[32];
+                tmem_ld32(lb + kColS + 32 * h, r);
+#pragma unroll
+                for (int g = 0; g < 8; ++g) {
+                    const float4 l4 = L4[8 * h + g];
+                    const float p0 = ex2_approx(fmaf(__uint_as_float(r[4 * g + 0]), c, -l4.x));
+                    const float p1 = ex2_approx(fmaf(__uint_as_float(r[4 * g + 1]), c, -l4.y));
+                    const float p2 = ex2_approx(fmaf(__uint_as_float(r[4 * g + 2]), c, -l4.z));
+                    const float p3 = ex2_approx(fmaf(__uint_as_float(r[4 * g + 3]), c, -l4.w));
+                    pk[16 * h + 2 * g] = pack_bf16x2(p0, p1);
+                    pk[16 * h + 2 * g + 1] = pack_bf16x2(p2, p3);
+                }
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t w[32];
+#pragma unroll
+                for (int x = 0; x < 32; ++x) w[x] = pk[32 * h + x];
+                tmem_st32(lb + kColS + 32 * h, w);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bars.p_full));
+
+            // dS^T = P^T o (dP^T - delta)
+            ok = mbar_wait(smem_u32(&bars.dp_full), i & 1, lim, &abort_flag);
+            if (ok && i >= 2) ok = mbar_wait(smem_u32(&bars.ds_empty[s]), ((i >> 1) & 1) ^ 1, lim, &abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            uint8_t* dsbuf = sb_ptr + kOffDS + s * kDSBytes;
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                uint32_t r[32];
+                tmem_ld32(lb + kColDP + 32 * h, r);
+                uint32_t w[16];
+#pragma unroll
+                for (int g = 0; g < 8; ++g) {
+                    const float4 d4 = D4[8 * h + g];
+                    const uint32_t pa = pk[16 * h + 2 * g], pb = pk[16 * h + 2 * g + 1];
+                    const float p0 = __uint_as_float(pa << 16), p1 = __uint_as_float(pa & 0xFFFF0000u);
+                    const float p2 = __uint_as_float(pb << 16), p3 = __uint_as_float(pb & 0xFFFF0000u);
+                    w[2 * g] = pack_bf16x2(p0 * (__uint_as_float(r[4 * g + 0]) - d4.x),
+                                           p1 * (__uint_as_float(r[4 * g + 1]) - d4.y));
+                    w[2 * g + 1] = pack_bf16x2(p2 * (__uint_as_float(r[4 * g + 2]) - d4.z),
+                                               p3 * (__uint_as_float(r[4 * g + 3]) - d4.w));
+                }
+                tmem_st16(lb + kColDP + 16 * h, w);
+                // queries 32h..32h+31 of this key row -> MN-major swizzled A tile for dQ:
+                // column (query / 64), row = key, 16-byte granule (query % 64) / 8 ^ (key % 8)
+                const int col = h >> 1;
+#pragma unroll
+                for (int g4 = 0; g4 < 4; ++g4) {
+                    const int gran = ((h & 1) * 4 + g4) ^ (key_in_blk & 7);
+                    uint4* dst = reinterpret_cast<uint4*>(dsbuf + col * 16384 + key_in_blk * 128 + gran * 16);
+                    *dst = make_uint4(w[4 * g4], w[4 * g4 + 1], w[4 * g4 + 2], w[4 * g4 + 3]);
+                }
+            }
+            tmem_st_wait();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bars.ds_full));
+        }
+        // epilogue: dV rows of this key block
+        if (ok) {
+            ok = mbar_wait(smem_u32(&bars.all_done), 0, lim, &abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+        }
+        if (!ok) {
+            if (lane == 0) record_timeout(args.ctl, &abort_flag);
+        } else {
+            tc_fence_after();
+            const int key = kvb * kBlk + key_in_blk;
+            uint16_t* out = static_cast<uint16_t*>(args.dv) + (static_cast<size_t>(bh) * N + key) * kD;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t r[32];
+                tmem_ld32(lb + kColDV + 32 * h, r);
+                if (key < N) {
+                    uint4* o4 = reinterpret_cast<uint4*>(out + 32 * h);
+#pragma unroll
+                    for (int x = 0; x < 4; ++x)
+                        o4[x] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * x]), __uint_as_float(r[8 * x + 1])),
+                                           pack_bf16x2(__uint_as_float(r[8 * x + 2]), __uint_as_float(r[8 * x + 3])),
+                                           pack_bf16x2(__uint_as_float(r[8 * x + 4]), __uint_as_float(r[8 * x + 5])),
+                                           pack_bf16x2(__uint_as_float(r[8 * x + 6]), __uint_as_float(r[8 * x + 7])));
+                }
+            }
+        }
+    } else if (warp >= 8) {
+        // ================================================================ dQ warpgroup
+        const int wq = warp % 4;
+        const int row_in_blk = wq * 32 + lane;
+        const uint32_t lb = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+        bool ok = true;
+        for (int i = 0; i < n_q; ++i) {
+            const int s = i & 1;
+            ok = mbar_wait(smem_u32(&bars.dq_full[s]), (i >> 1) & 1, lim, &abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t r[2][32];
+            tmem_ld32(lb + kColDQ + 64 * s, r[0]);
+            tmem_ld32(lb + kColDQ + 64 * s + 32, r[1]);
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bars.dq_free[s]));
+            float* acc = args.dq_acc + (static_cast<size_t>(bh) * Np + static_cast<size_t>(i) * kBlk + row_in_blk) * kD;
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int x = 0; x < 8; ++x)
+                    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(acc + 32 * h + 4 * x),
+                                 "f"(__uint_as_float(r[h][4 * x])), "f"(__uint_as_float(r[h][4 * x + 1])),
+                                 "f"(__uint_as_float(r[h][4 * x + 2])), "f"(__uint_as_float(r[h][4 * x + 3]))
+                                 : "memory");
+        }
+        // epilogue: dK rows of this key block, times scale
+        if (ok) {
+            ok = mbar_wait(smem_u32(&bars.all_done), 0, lim, &abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+        }
+        if (!ok) {
+            if (lane == 0) record_timeout(args.ctl, &abort_flag);
+        } else {
+            tc_fence_after();
+            const int key = kvb * kBlk + row_in_blk;
+            const float sc = args.scale;
+            uint16_t* out = static_cast<uint16_t*>(args.dk) + (static_cast<size_t>(bh) * N + key) * kD;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t r[32];
+                tmem_ld32(lb + kColDK + 32 * h, r);
+                if (key < N) {
+                    uint4* o4 = reinterpret_cast<uint4*>(out + 32 * h);
+#pragma unroll
+                    for (int x = 0; x < 4; ++x)
+                        o4[x] = make_uint4(
+                            pack_bf16x2(__uint_as_float(r[8 * x]) * sc, __uint_as_float(r[8 * x + 1]) * sc),
+                            pack_bf16x2(__uint_as_float(r[8 * x + 2]) * sc, __uint_as_float(r[8 * x + 3]) * sc),
+                            pack_bf16x2(__uint_as_float(r[8 * x + 4]) * sc, __uint_as_float(r[8 * x + 5]) * sc),
+                            pack_bf16x2(__uint_as_float(r[8 * x + 6]) * sc, __uint_as_float(r[8 * x + 7]) * sc));
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------- pre / post passes
+// delta_i = dO_i . O_i, lse2_i = lse_i * log2(e) (rows past N: delta 0, lse2 +inf
+// so that recomputed P is exactly 0 there), dQ accumulator zeroed.
+// 8 threads per row, each reading 16 bytes of O and dO.
+__global__ void bwd_prep_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dO,
+                                const float* __restrict__ lse, float* __restrict__ ws_delta,
+                                float* __restrict__ ws_lse2, float4* __restrict__ dq_acc, int BH,
+                                int N, int Np, size_t acc_vec4) {
+    const size_t tid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const size_t nthreads = static_cast<size_t>(gridDim.x) * blockDim.x;
+    const size_t rows = static_cast<size_t>(BH) * Np;
+    for (size_t base = tid; base < rows * 8; base += nthreads) {
+        const size_t r = base / 8;
+        const int part = static_cast<int>(base % 8);
+        const int bh = static_cast<int>(r / Np), i = static_cast<int>(r % Np);
+        float sum = 0.f;
+        if (i < N) {
+            const size_t src = (static_cast<size_t>(bh) * N + i) * 8 + part;
+            const uint4 a = o[src], b = dO[src];
+            const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+                sum = fmaf(__uint_as_float(av[x] << 16), __uint_as_float(bv[x] << 16), sum);
+                sum = fmaf(__uint_as_float(av[x] & 0xFFFF0000u), __uint_as_float(bv[x] & 0xFFFF0000u), sum);
+            }
+        }
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+        if (part == 0) {
+            ws_delta[r] = sum;
+            ws_lse2[r] = (i < N) ? lse[static_cast<size_t>(bh) * N + i] * kLog2e : INFINITY;
+        }
+    }
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (size_t x = tid; x < acc_vec4; x += nthreads) dq_acc[x] = z;
+}
+
+// dQ = bf16(scale * accumulator) for rows < N; 8 elements per thread.
+__global__ void bwd_dq_convert_kernel(const float4* __restrict__ acc, uint4* __restrict__ dq,
+                                      int N, int Np, size_t n_vec8, float scale) {
+    const size_t tid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const size_t nthreads = static_cast<size_t>(gridDim.x) * blockDim.x;
+    constexpr int kVecPerRow = kD / 8;
+    for (size_t x = tid; x < n_vec8; x += nthreads) {
+        const size_t row = x / kVecPerRow;  // row in [BH][N]
+        const int part = static_cast<int>(x % kVecPerRow);
+        const size_t bh = row / N, i = row % N;
+        const size_t src = ((bh * Np + i) * kVecPerRow + part) * 2;
+        const float4 a = acc[src], b = acc[src + 1];
+        dq[x] = make_uint4(pack_bf16x2(a.x * scale, a.y * scale), pack_bf16x2(a.z * scale, a.w * scale),
+                           pack_bf16x2(b.x * scale, b.y * scale), pack_bf16x2(b.z * scale, b.w * scale));
+    }
+}
+
+int grid_for(size_t work, int threads, int max_blocks) {
+    size_t b = (work + threads - 1) / threads;
+    if (b > static_cast<size_t>(max_blocks)) b = max_blocks;
+    return static_cast<int>(b < 1 ? 1 : b);
+}
+
+}  // namespace
+
+size_t bwd_workspace_bytes(int BH, int N, int d) {
+    const size_t Np = static_cast<size_t>(round_up(N, kBlk));
+    return (2 * static_cast<size_t>(BH) * Np + static_cast<size_t>(BH) * Np * d) * sizeof(float);
+}
+
+int launch_bwd_sm103(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                     const void* dO, void* dq, void* dk, void* dv, void* workspace, int BH, int N,
+                     int d, float scale, DevCtl ctl, cudaStream_t s) {
+    if (d != kD) return -1;
+    const int Np = round_up(N, kBlk);
+    float* ws = static_cast<float*>(workspace);
+    float* ws_delta = ws;
+    float* ws_lse2 = ws + static_cast<size_t>(BH) * Np;
+    float* dq_acc = ws + 2 * static_cast<size_t>(BH) * Np;
+    const size_t acc_vec4 = static_cast<size_t>(BH) * Np * kD / 4;
+
+    int sms = 152;
+    {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    }
+    bwd_prep_kernel<<<grid_for(static_cast<size_t>(BH) * Np * 8, 256, sms * 8), 256, 0, s>>>(
+        static_cast<const uint4*>(o), static_cast<const uint4*>(dO), lse, ws_delta, ws_lse2,
+        reinterpret_cast<float4*>(dq_acc), BH, N, Np, acc_vec4);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return static_cast<int>(e);
+
+    CUtensorMap tq, tk, tv, tdo;
+    const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    int rc = make_map_3d(&tq, q, dt, 2, kD, N, BH, 64, kBlk);
+    if (rc == 0) rc = make_map_3d(&tk, k, dt, 2, kD, N, BH, 64, kBlk);
+    if (rc == 0) rc = make_map_3d(&tv, v, dt, 2, kD, N, BH, 64, kBlk);
+    if (rc == 0) rc = make_map_3d(&tdo, dO, dt, 2, kD, N, BH, 64, kBlk);
+    if (rc != 0) return rc;
+    static uint64_t attr_set = 0;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 64 || !(attr_set & (1ull << dev))) {
+        e = cudaFuncSetAttribute(bwd_main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+        if (e != cudaSuccess) return static_cast<int>(e);
+        if (dev < 64) attr_set |= 1ull << dev;
+    }
+    BwdArgs a;
+    a.ws_delta = ws_delta;
+    a.ws_lse2 = ws_lse2;
+    a.dq_acc = dq_acc;
+    a.dk = dk;
+    a.dv = dv;
+    a.N = N;
+    a.Np = Np;
+    a.n_kv = Np / kBlk;
+    a.c_log2 = scale * kLog2e;
+    a.scale = scale;
+    a.ctl = ctl;
+    bwd_main_kernel<<<a.n_kv * BH, kThreads, kSmemAlloc, s>>>(tq, tk, tv, tdo, a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return static_cast<int>(e);
+
+    const size_t n_vec8 = static_cast<size_t>(BH) * N * kD / 8;
+    bwd_dq_convert_kernel<<<grid_for(n_vec8, 256, sms * 8), 256, 0, s>>>(
+        reinterpret_cast<const float4*>(dq_acc), static_cast<uint4*>(dq), N, Np, n_vec8, scale);
+    return static_cast<int>(cudaGetLastError());
+}
+
+}  // namespace fa

@@ -1,0 +1,478 @@
+// fwd_sm103.cu -- attention forward on the sm_103a tensor core (tcgen05 + TMEM + TMA).
+//
+// What it computes is the online-softmax forward of the "FlashAttention-1"
+// page (10.2.2-10.2.3) in the unnormalised form of the "5.4 FlashAttention"
+// page's listing 3-1 and the Python demo of the "Flash Attention V1/V2/V3演进"
+// page: per query row a running max m, a running sum l and an unnormalised
+// output o; each K/V block rescales the old state by alpha = exp(m_old - m_new)
+// and adds exp(S - m_new) V; o / l once at the end; lse = m + ln l is saved for
+// the backward.  Work split as the V2 section describes (one CTA owns its query
+// rows and sweeps all K/V blocks, so O is final after one pass); scale and log2(e)
+// are folded into one multiply before exp2, and the causal mask is applied in
+// the score step.
+//
+// GB300 design (not the A100/H100 designs the pages sketch):
+//   * CTA = 2 query tiles of 128 rows (one head), 12 warps:
+//       warp 0      TMA producer: Q once, then K_j / V_j into 2-stage rings
+//       warp 1      MMA issuer (one thread) + TMEM owner
+//       warps 4-7   softmax for query tile 0, warps 8-11 for query tile 1
+//   * TMEM (512 columns): S_t (128 fp32 columns per tile), O_t (d columns);
+//     P_t is written back over S_t as bf16 (or E4M3) and fed to the P V MMA
+//     straight from TMEM.
+//   * MMA order per K/V block j: O_0 += P_0 V_j, S_0 = Q_0 K_{j+1}^T,
+//     O_1 += P_1 V_j, S_1 = Q_1 K_{j+1}^T -- the two softmax warpgroups
+//     alternate with the tensor core (ping-pong).  MMAs issued by one thread
+//     run in order, so the commit that publishes S_t(j+1) also proves that
+//     O_t += P_t(j) V_j is finished; the softmax warps may then rescale O_t.
+//   * Lazy rescale: the reference max used for exp2 moves only when a row's
+//     block max exceeds it by more than kTau (log2 units).  O and l always share
+//     the same reference, so the result is exact for any threshold; p stays
+//     <= 2^kTau (fine for bf16 and below the E4M3 limit of 448).
+//   * Every wait is bounded; on a timeout the kernel records it, drains its own
+//     TMA loads and MMAs, frees TMEM and exits.
+#include <cmath>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "tma_host.h"
+
+namespace fa {
+namespace {
+
+constexpr int kBM = 128;         // query rows per tile
+constexpr int kBN = 128;         // keys per K/V block
+constexpr int kStages = 2;       // K ring and V ring depth
+constexpr int kThreads = 384;    // 12 warps
+constexpr float kTau = 8.0f;     // lazy-rescale threshold, log2 units
+
+struct FwdArgs {
+    void* o;
+    float* lse;
+    int N;
+    int n_pairs;      // query-tile pairs per head
+    float c_log2;     // scale * log2(e) (times the FP8 descales)
+    float o_scale;    // multiplies O at the end (FP8: v descale), 1 otherwise
+    int causal;
+    DevCtl ctl;
+};
+
+template <int D, bool FP8>
+struct Cfg {
+    static constexpr int kElem = FP8 ? 1 : 2;
+    static constexpr int kRowBytes = D * kElem;
+    static constexpr int kChunks = kRowBytes / 128;        // 128-byte swizzle columns
+    static constexpr int kBoxX = 128 / kElem;              // elements per chunk row
+    static constexpr int kChunkBytes = 128 * 128;          // 128 rows x 128 B
+    static constexpr int kTileBytes = kChunks * kChunkBytes;
+    static constexpr int kKStep = FP8 ? 32 : 16;           // K per MMA
+    static constexpr int kStepBytes = kKStep * kElem;      // = 32
+    // shared memory: Q0, Q1, K[kStages], V[kStages]
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffK = 2 * kTileBytes;
+    static constexpr int kOffV = kOffK + kStages * kTileBytes;
+    static constexpr int kSmemBytes = kOffV + kStages * kTileBytes;
+    static constexpr int kSmemAlloc = kSmemBytes + 1024;   // slack for 1 KB alignment
+    // TMEM columns
+    static constexpr uint32_t kColS0 = 0, kColS1 = 128;
+    static constexpr uint32_t kColO0 = 256, kColO1 = 256 + D;
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kIdescS = FP8 ? idesc_e4m3(kBM, kBN, false, false)
+                                            : idesc_bf16(kBM, kBN, false, false);
+    static constexpr uint32_t kIdescO = FP8 ? idesc_e4m3(kBM, D, false, true)
+                                            : idesc_bf16(kBM, D, false, true);
+};
+
+struct Bars {
+    uint64_t q_full;
+    uint64_t k_full[kStages], k_empty[kStages];
+    uint64_t v_full[kStages], v_empty[kStages];
+    uint64_t s_full[2], p_full[2], o_done[2];
+    uint64_t drain;
+};
+
+__device__ __forceinline__ void record_timeout(const DevCtl& ctl, volatile int* abort_flag) {
+    *abort_flag = 1;
+    atomicCAS(ctl.status, kDevOk, kDevTimeout);
+}
+
+// Keep the compiler from using TMEM-load results before the wait instruction.
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(r[i]));
+}
+
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+template <int D, bool FP8>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const FwdArgs args) {
+    using C = Cfg<D, FP8>;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) Bars bars;
+    __shared__ uint32_t tmem_slot;
+    __shared__ volatile int abort_flag;
+
+    const uint32_t smem_base =
+        (smem_u32(smem_raw) + 1023u) & ~1023u;  // 1 KB aligned for the 128 B swizzle
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+    // ---- tile coordinates: within a head, heaviest (last) query pair first
+    const int bh = blockIdx.x / args.n_pairs;
+    const int pair = args.n_pairs - 1 - (blockIdx.x % args.n_pairs);
+    const int r0 = pair * 2 * kBM;
+    const int N = args.N;
+    const int kv_end = args.causal ? min(N, r0 + 2 * kBM) : N;
+    const int n_kv = (kv_end + kBN - 1) / kBN;
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(smem_u32(&bars.q_full), 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(&bars.k_full[s]), 1);
+            mbar_init(smem_u32(&bars.k_empty[s]), 1);
+            mbar_init(smem_u32(&bars.v_full[s]), 1);
+            mbar_init(smem_u32(&bars.v_empty[s]), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(smem_u32(&bars.s_full[t]), 1);
+            mbar_init(smem_u32(&bars.p_full[t]), 128);
+            mbar_init(smem_u32(&bars.o_done[t]), 1);
+        }
+        mbar_init(smem_u32(&bars.drain), 1);
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&tmem_slot), C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    const uint64_t lim = args.ctl.wait_ns;
+
+    if (warp == 0) {
+        // ================================================================ TMA producer
+        if (lane == 0) {
+            const uint32_t qf = smem_u32(&bars.q_full);
+            mbar_arrive_expect_tx(qf, 2 * C::kTileBytes);
+            for (int t = 0; t < 2; ++t)
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_3d(smem_base + C::kOffQ + t * C::kTileBytes + c * C::kChunkBytes, &tm_q,
+                                qf, c * C::kBoxX, r0 + t * kBM, bh);
+            int issued = 0;
+            bool ok = true;
+            for (int j = 0; j < n_kv && ok; ++j) {
+                const int s = j % kStages;
+                const uint32_t ph = ((j / kStages) & 1) ^ 1;
+                if (j >= kStages && !mbar_wait(smem_u32(&bars.k_empty[s]), ph, lim, &abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t kf = smem_u32(&bars.k_full[s]);
+                mbar_arrive_expect_tx(kf, C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_3d(smem_base + C::kOffK + s * C::kTileBytes + c * C::kChunkBytes, &tm_k,
+                                kf, c * C::kBoxX, j * kBN, bh);
+                if (j >= kStages && !mbar_wait(smem_u32(&bars.v_empty[s]), ph, lim, &abort_flag)) {
+                    issued = 2 * j + 1;
+                    ok = false;
+                    break;
+                }
+                const uint32_t vf = smem_u32(&bars.v_full[s]);
+                mbar_arrive_expect_tx(vf, C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_3d(smem_base + C::kOffV + s * C::kTileBytes + c * C::kChunkBytes, &tm_v,
+                                vf, c * C::kBoxX, j * kBN, bh);
+                issued = 2 * j + 2;
+            }
+            if (!ok) record_timeout(args.ctl, &abort_flag);
+            // drain: Q and the newest load of every stage have landed before exit
+            const volatile int never = 0;
+            mbar_wait(qf, 0, kDrainWaitNs, &never);
+            for (int x = max(0, issued - 2 * kStages); x < issued; ++x) {
+                const int j = x / 2;
+                const int s = j % kStages;
+                const uint32_t bar = (x & 1) ? smem_u32(&bars.v_full[s]) : smem_u32(&bars.k_full[s]);
+                mbar_wait(bar, (j / kStages) & 1, kDrainWaitNs, &never);
+            }
+        }
+    } else if (warp == 1) {
+        // ================================================================ MMA issuer
+        if (lane == 0) {
+            const uint32_t sQ0 = smem_base + C::kOffQ, sQ1 = sQ0 + C::kTileBytes;
+            bool ok = mbar_wait(smem_u32(&bars.q_full), 0, lim, &abort_flag);
+            auto issue_s = [&](uint32_t sQ, int s, uint32_t col) {
+                const uint32_t sK = smem_base + C::kOffK + s * C::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < D / C::kKStep; ++kk) {
+                    const uint32_t off = (kk * C::kStepBytes) / 128 * C::kChunkBytes +
+                                         (kk * C::kStepBytes) % 128;
+                    const uint64_t da = sdesc_sw128(sQ + off, 16, 1024);
+                    const uint64_t db = sdesc_sw128(sK + off, 16, 1024);
+                    if (FP8)
+                        mma_e4m3_ss(tmem + col, da, db, C::kIdescS, kk > 0);
+                    else
+                        mma_bf16_ss(tmem + col, da, db, C::kIdescS, kk > 0);
+                }
+            };
+            auto issue_pv = [&](uint32_t colP, int s, uint32_t colO, bool acc) {
+                const uint32_t sV = smem_base + C::kOffV + s * C::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < kBN / C::kKStep; ++kk) {
+                    const uint64_t db = sdesc_sw128(sV + kk * C::kKStep * 128, C::kChunkBytes, 1024);
+                    if (FP8)
+                        mma_e4m3_ts(tmem + colO, tmem + colP + kk * 8, db, C::kIdescO, acc || kk > 0);
+                    else
+                        mma_bf16_ts(tmem + colO, tmem + colP + kk * 8, db, C::kIdescO, acc || kk > 0);
+                }
+            };
+            if (ok) ok = mbar_wait(smem_u32(&bars.k_full[0]), 0, lim, &abort_flag);
+            if (ok) {
+                tc_fence_after();
+                issue_s(sQ0, 0, C::kColS0);
+                mma_commit(smem_u32(&bars.s_full[0]));
+                issue_s(sQ1, 0, C::kColS1);
+                mma_commit(smem_u32(&bars.s_full[1]));
+                mma_commit(smem_u32(&bars.k_empty[0]));
+            }
+            for (int j = 0; j < n_kv && ok; ++j) {
+                const int s = j % kStages;
+                const uint32_t ph = (j / kStages) & 1;
+                const int s1 = (j + 1) % kStages;
+                const uint32_t ph1 = ((j + 1) / kStages) & 1;
+                const bool more = (j + 1 < n_kv);
+                ok = mbar_wait(smem_u32(&bars.v_full[s]), ph, lim, &abort_flag);
+                if (ok) ok = mbar_wait(smem_u32(&bars.p_full[0]), j & 1, lim, &abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+                issue_pv(C::kColS0, s, C::kColO0, j > 0);
+                if (more) {
+                    ok = mbar_wait(smem_u32(&bars.k_full[s1]), ph1, lim, &abort_flag);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_s(sQ0, s1, C::kColS0);
+                    mma_commit(smem_u32(&bars.s_full[0]));
+                } else {
+                    mma_commit(smem_u32(&bars.o_done[0]));
+                }
+                ok = mbar_wait(smem_u32(&bars.p_full[1]), j & 1, lim, &abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+                issue_pv(C::kColS1, s, C::kColO1, j > 0);
+                mma_commit(smem_u32(&bars.v_empty[s]));
+                if (more) {
+                    issue_s(sQ1, s1, C::kColS1);
+                    mma_commit(smem_u32(&bars.s_full[1]));
+                    mma_commit(smem_u32(&bars.k_empty[s1]));
+                } else {
+                    mma_commit(smem_u32(&bars.o_done[1]));
+                }
+            }
+            if (!ok) record_timeout(args.ctl, &abort_flag);
+            // drain every MMA this thread issued before TMEM is released
+            mma_commit(smem_u32(&bars.drain));
+            const volatile int never = 0;
+            mbar_wait(smem_u32(&bars.drain), 0, kDrainWaitNs, &never);
+        }
+    } else if (warp >= 4) {
+        // ================================================================ softmax warpgroups
+        const int t = (warp - 4) / 4;              // query tile 0 or 1
+        const int wq = warp % 4;                   // TMEM lane quarter
+        const int row_in_tile = wq * 32 + lane;
+        const int qrow = r0 + t * kBM + row_in_tile;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+        const uint32_t colS = t ? C::kColS1 : C::kColS0;
+        const uint32_t colO = t ? C::kColO1 : C::kColO0;
+        const float c = args.c_log2;
+        float m_ref = -INFINITY;  // reference max in log2 units
+        float l = 0.f;
+        bool ok = true;
+
+        for (int j = 0; j < n_kv; ++j) {
+            ok = mbar_wait(smem_u32(&bars.s_full[t]), j & 1, lim, &abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t r[4][32];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) tmem_ld32_nowait(lane_base + colS + 32 * q4, r[q4]);
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) reg_fence(r[q4]);
+
+            float x[128];
+            const int kv0 = j * kBN;
+            const bool need_mask = (kv0 + kBN > N) || (args.causal && kv0 + kBN - 1 > qrow);
+            float mt = -INFINITY;
+            if (need_mask) {
+#pragma unroll
+                for (int i = 0; i < 128; ++i) {
+                    const int key = kv0 + i;
+                    const bool masked = key >= N || (args.causal && key > qrow);
+                    x[i] = masked ? -INFINITY : __uint_as_float(r[i / 32][i % 32]) * c;
+                    mt = fmaxf(mt, x[i]);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 128; ++i) {
+                    x[i] = __uint_as_float(r[i / 32][i % 32]) * c;
+                    mt = fmaxf(mt, x[i]);
+                }
+            }
+            // lazy rescale: move the reference only when the block max exceeds it by > kTau
+            float alpha = 1.f;
+            const bool bump = mt > m_ref + kTau;
+            if (bump) {
+                alpha = (m_ref == -INFINITY) ? 0.f : ex2_approx(m_ref - mt);
+                m_ref = mt;
+                l *= alpha;
+            }
+            if (j > 0 && __any_sync(0xffffffffu, bump)) {
+                // O_t += P V of the previous block has completed (it precedes S_t(j) in
+                // issue order), so O_t can be rescaled in place.
+#pragma unroll
+                for (int q4 = 0; q4 < D / 32; ++q4) {
+                    uint32_t ov[32];
+                    tmem_ld32(lane_base + colO + 32 * q4, ov);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                    tmem_st32(lane_base + colO + 32 * q4, ov);
+                }
+            }
+            const float ref = (m_ref == -INFINITY) ? 0.f : m_ref;
+            float rs = 0.f;
+            if (FP8) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float p0 = ex2_approx(x[4 * i] - ref), p1 = ex2_approx(x[4 * i + 1] - ref);
+                    const float p2 = ex2_approx(x[4 * i + 2] - ref), p3 = ex2_approx(x[4 * i + 3] - ref);
+                    rs += (p0 + p1) + (p2 + p3);
+                    pk[i] = pack_e4m3x4(p0, p1, p2, p3);
+                }
+                tmem_st32(lane_base + colS, pk);
+            } else {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float p0 = ex2_approx(x[64 * h + 2 * i] - ref);
+                        const float p1 = ex2_approx(x[64 * h + 2 * i + 1] - ref);
+                        rs += p0 + p1;
+                        pk[i] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st32(lane_base + colS + 32 * h, pk);
+                }
+            }
+            l += rs;
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bars.p_full[t]));
+        }
+        if (ok) {
+            ok = mbar_wait(smem_u32(&bars.o_done[t]), 0, lim, &abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+        }
+        if (!ok) {
+            if (lane == 0) record_timeout(args.ctl, &abort_flag);
+        } else {
+            tc_fence_after();
+            const float inv = args.o_scale / l;
+            const size_t orow = (static_cast<size_t>(bh) * N + qrow) * D;
+#pragma unroll
+            for (int q4 = 0; q4 < D / 32; ++q4) {
+                uint32_t ov[32];
+                tmem_ld32(lane_base + colO + 32 * q4, ov);
+                if (qrow < N) {
+                    uint32_t w[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        w[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv,
+                                           __uint_as_float(ov[2 * i + 1]) * inv);
+                    uint4* out = reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.o) + orow + 32 * q4);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        out[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                }
+            }
+            if (qrow < N && args.lse != nullptr)
+                args.lse[static_cast<size_t>(bh) * N + qrow] = (m_ref + log2f(l)) * 0.69314718055994530942f;
+        }
+    }
+    // warps 2-3 have no role
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+template <int D, bool FP8>
+int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse, int BH, int N,
+                float c_log2, float o_scale, int causal, DevCtl ctl, cudaStream_t s) {
+    using C = Cfg<D, FP8>;
+    const CUtensorMapDataType dt =
+        FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    CUtensorMap tq, tk, tv;
+    int rc = make_map_3d(&tq, q, dt, C::kElem, D, N, BH, C::kBoxX, kBM);
+    if (rc == 0) rc = make_map_3d(&tk, k, dt, C::kElem, D, N, BH, C::kBoxX, kBN);
+    if (rc == 0) rc = make_map_3d(&tv, v, dt, C::kElem, D, N, BH, C::kBoxX, kBN);
+    if (rc != 0) return rc;
+    static uint64_t attr_set = 0;  // per template instance, one bit per device
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 64 || !(attr_set & (1ull << dev))) {
+        cudaError_t e = cudaFuncSetAttribute(fwd_sm103_kernel<D, FP8>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::kSmemAlloc);
+        if (e != cudaSuccess) return static_cast<int>(e);
+        if (dev < 64) attr_set |= 1ull << dev;
+    }
+    FwdArgs a;
+    a.o = o;
+    a.lse = lse;
+    a.N = N;
+    a.n_pairs = (N + 2 * kBM - 1) / (2 * kBM);
+    a.c_log2 = c_log2;
+    a.o_scale = o_scale;
+    a.causal = causal;
+    a.ctl = ctl;
+    dim3 grid(a.n_pairs * BH);
+    fwd_sm103_kernel<D, FP8><<<grid, kThreads, C::kSmemAlloc, s>>>(tq, tk, tv, a);
+    return static_cast<int>(cudaGetLastError());
+}
+
+}  // namespace
+
+int launch_fwd_sm103(const void* q, const void* k, const void* v, void* o, float* lse, int BH,
+                     int N, int d, float c_log2, float o_scale, int causal, bool is_fp8,
+                     DevCtl ctl, cudaStream_t s) {
+    if (is_fp8) return launch_impl<128, true>(q, k, v, o, lse, BH, N, c_log2, o_scale, causal, ctl, s);
+    if (d == 64) return launch_impl<64, false>(q, k, v, o, lse, BH, N, c_log2, o_scale, causal, ctl, s);
+    return launch_impl<128, false>(q, k, v, o, lse, BH, N, c_log2, o_scale, causal, ctl, s);
+}
+
+}  // namespace fa

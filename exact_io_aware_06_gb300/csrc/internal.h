@@ -1,0 +1,49 @@
+// internal.h -- declarations shared by the library's translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+// Device-side error codes written into the per-device status word.
+constexpr int kDevOk = 0;
+constexpr int kDevTimeout = 4;  // == FA_ERR_DEVICE_TIMEOUT
+
+// A single wait that runs out after this long records kDevTimeout; draining a
+// kernel's own in-flight copies / MMAs after that uses a fixed bound.
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+constexpr uint64_t kDrainWaitNs = 1000000000ull;
+
+struct DevCtl {
+    int* status;       // per-device status word (first error wins)
+    uint64_t wait_ns;  // bound on one wait
+};
+
+// fp32 exact forward on CUDA cores, d in {64, 128}.
+cudaError_t launch_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse,
+                           int BH, int N, int d, float scale, int causal, cudaStream_t s);
+
+// tcgen05 forward: bf16 (is_fp8 = false) or E4M3 inputs (is_fp8 = true, d = 128).
+// Returns 0 on success, or a CUDA / tensor-map error code (non-zero).
+int launch_fwd_sm103(const void* q, const void* k, const void* v, void* o, float* lse, int BH,
+                     int N, int d, float score_scale_log2, float o_scale, int causal, bool is_fp8,
+                     DevCtl ctl, cudaStream_t s);
+
+// Backward pieces.  Workspace layout (all float32, Np = N rounded up to 128):
+//   [0, BH*Np)            delta_i = dO_i . O_i
+//   [BH*Np, 2*BH*Np)      lse_i * log2(e)
+//   [2*BH*Np, ...)        dQ accumulator [BH][Np][d]
+size_t bwd_workspace_bytes(int BH, int N, int d);
+int launch_bwd_sm103(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                     const void* dO, void* dq, void* dk, void* dv, void* workspace, int BH, int N,
+                     int d, float scale, DevCtl ctl, cudaStream_t s);
+
+// A kernel that waits on a barrier nobody arrives at, with the bounded wait;
+// it must record kDevTimeout and return.
+cudaError_t launch_wait_selftest(DevCtl ctl, cudaStream_t s);
+
+inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
+
+}  // namespace fa

@@ -1,0 +1,162 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) exact-attention library, libfa.so.
+ *
+ * The operation is exact scaled-dot-product attention computed tile by tile
+ * with online softmax, so the N x N score and probability matrices never reach
+ * device memory:
+ *
+ *     S = scale * Q K^T  (causal: S_ij = -inf for key j > query i),
+ *     P = rowsoftmax(S),  O = P V,  lse_i = log sum_j exp(S_ij)
+ *
+ * ("FlashAttention-1", jshn9515 deep-learning-notes 10.2.1-10.2.3, for the
+ * definition and the online-softmax rescaling; "Flash Attention V1/V2/V3演进",
+ * sections V1分块原理 / 在线Softmax / V2并行优化, for tiling, the running
+ * max/sum/output state and the one-time final normalisation; "5.4
+ * FlashAttention", listing 3-1, for the alpha = exp(m_old - m_new) rescale.)
+ * The backward recomputes P from the saved lse instead of storing it
+ * ("FlashAttention-1", 10.2.4).
+ *
+ * Conventions shared by every entry point
+ *   - Tensors are dense, contiguous, row-major [B][H][N][d]; lse and delta are
+ *     [B][H][N].  There are no strides.  Every device pointer must be 16-byte
+ *     aligned (tensor-memory-accelerator copies need it); a misaligned pointer
+ *     is FA_ERR_INVALID_ARG.
+ *   - All pointers are DEVICE pointers on the current CUDA device unless a
+ *     comment says otherwise.  The caller owns every buffer, including the
+ *     backward workspace; the library allocates no device memory per call.  It
+ *     owns only one status word per device, created on first use.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls are asynchronous on that stream: they enqueue kernels and
+ *     return without synchronising.
+ *   - Return value: an fa_status.  Argument problems are detected on the host
+ *     before anything is launched.  Errors that happen inside a kernel (a
+ *     bounded wait that ran out) are recorded in the per-device status word and
+ *     reported by fa_last_device_error().
+ *   - `scale` multiplies Q K^T (the configurations use 1/sqrt(d)).
+ *   - Any N >= 1 is accepted (tiles past N are zero-filled and masked).
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { FA_F32 = 0, FA_BF16 = 1, FA_E4M3 = 2 } fa_dtype;
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,     /* null/misaligned pointer, N < 1, B/H < 1, bad dtype */
+    FA_ERR_UNSUPPORTED = 2,     /* valid request this build does not implement      */
+    FA_ERR_CUDA = 3,            /* a CUDA runtime/driver call or launch failed      */
+    FA_ERR_DEVICE_TIMEOUT = 4   /* a kernel's bounded wait ran out (device-side)    */
+} fa_status;
+
+/*
+ * Forward pass.  O = softmax(scale Q K^T [causal mask]) V and
+ * lse_i = m_i + ln l_i (natural log, in units of the scaled score; m_i the row
+ * max, l_i the row sum of exp(S_ij - m_i)), as on the "FlashAttention-1" page
+ * 10.2.1 (standard attention, stable softmax) and 10.2.2 (online update).
+ *
+ *   q, k, v : [B][H][N][d] of `dtype`, read only.
+ *   o       : [B][H][N][d] of `dtype`, written (fully overwritten).
+ *   lse     : [B][H][N] float32, written.  May be NULL if not wanted.
+ *   dtype   : FA_F32 (d = 64 or 128; exact fp32 CUDA-core kernel) or
+ *             FA_BF16 (d = 64 or 128; tensor-core kernel with fp32
+ *             accumulation; O rounded to bf16 to nearest even).
+ *             FA_E4M3 is FA_ERR_INVALID_ARG here: use fa_fwd_fp8().
+ *   causal  : 0 = full attention; 1 = key j attends only to queries i >= j.
+ * Errors: FA_ERR_INVALID_ARG (null q/k/v/o, misalignment, B,H,N < 1, bad
+ * dtype), FA_ERR_UNSUPPORTED (other d), FA_ERR_CUDA (launch failure).
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+           int B, int H, int N, int d, float scale, int causal, int dtype, void* stream);
+
+/*
+ * FP8 forward ("Flash Attention V1/V2/V3演进", section V3增强: FP8 matrix
+ * inputs, FP32 accumulation, scale factors).  Inputs are OCP E4M3 codes with
+ * one float32 dequantisation factor per tensor: the real value of element x is
+ * e4m3(x) * x_descale.  The kernel computes the same O and lse as fa_fwd on the
+ * dequantised inputs; P is re-quantised to E4M3 inside the kernel for the P V
+ * product (accumulation stays fp32).
+ *
+ *   q8, k8, v8 : [B][H][N][d] uint8 E4M3 codes.
+ *   o          : [B][H][N][d] bfloat16, written.
+ *   lse        : [B][H][N] float32, written (may be NULL).
+ *   d          : 128.
+ * Errors: as fa_fwd; FA_ERR_INVALID_ARG also for a non-finite or <= 0 descale.
+ */
+int fa_fwd_fp8(const void* q8, const void* k8, const void* v8, void* o, float* lse,
+               float q_descale, float k_descale, float v_descale,
+               int B, int H, int N, int d, float scale, int causal, void* stream);
+
+/*
+ * Bytes of device workspace that fa_bwd needs for these sizes: the per-row
+ * delta_i = dO_i . O_i and the pre-scaled lse (float32, N rounded up to 128
+ * per head) and the float32 dQ accumulator ([B][H][N rounded up to 128][d]).
+ * Returns 0 for invalid sizes.
+ */
+size_t fa_bwd_workspace_size(int B, int H, int N, int d);
+
+/*
+ * Backward pass by recomputation ("FlashAttention-1", 10.2.4): with
+ * P_ij = exp(S_ij - lse_i) rebuilt tile by tile from the saved lse,
+ *     dV = P^T dO,   dP = dO V^T,   delta_i = dO_i . O_i,
+ *     dS = P o (dP - delta),   dQ = scale dS K,   dK = scale dS^T Q.
+ *
+ *   q, k, v, o, dO : [B][H][N][d] bfloat16, read only (o from fa_fwd).
+ *   lse            : [B][H][N] float32 from fa_fwd, read only.
+ *   dq, dk, dv     : [B][H][N][d] bfloat16, written.
+ *   workspace      : device buffer of at least fa_bwd_workspace_size() bytes,
+ *                    owned by the caller; its contents on entry do not matter
+ *                    and on return are unspecified.  Calls that overlap in time
+ *                    must not share one workspace.
+ *   dtype          : FA_BF16.   d : 64.   causal : 0.
+ * Errors: FA_ERR_INVALID_ARG (null/misaligned pointers, workspace too small,
+ * bad sizes), FA_ERR_UNSUPPORTED (other dtype or d, causal = 1),
+ * FA_ERR_CUDA (launch failure).
+ */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+           const void* dO, void* dq, void* dk, void* dv, void* workspace,
+           size_t workspace_bytes, int B, int H, int N, int d, float scale, int causal,
+           int dtype, void* stream);
+
+/*
+ * Synchronise `stream`, then return and clear the current device's status
+ * word: FA_OK, or the first device-side error recorded since the last call
+ * (FA_ERR_DEVICE_TIMEOUT when a kernel's bounded wait ran out; that kernel
+ * returned early and its outputs are undefined).  FA_ERR_CUDA if the
+ * synchronisation itself failed.
+ */
+int fa_last_device_error(void* stream);
+
+/*
+ * Upper bound, in nanoseconds of %globaltimer, on any single wait inside a
+ * kernel launched after this call on any device (default 2e9 = 2 s; 0 restores
+ * the default).  After it runs out the kernel records FA_ERR_DEVICE_TIMEOUT,
+ * drains its own in-flight copies and matrix operations (with a fixed 1 s
+ * bound), frees its tensor memory and returns.  Tests use a tiny limit to
+ * exercise that path; it is not a tuning knob.
+ */
+void fa_set_wait_timeout_ns(uint64_t ns);
+
+/*
+ * Failure-path self test: launch a one-warp kernel whose single wait can never
+ * be satisfied (nothing arrives on its barrier).  The bounded wait gives up
+ * after the fa_set_wait_timeout_ns() limit and records FA_ERR_DEVICE_TIMEOUT,
+ * which the next fa_last_device_error() returns.  Nothing faults or hangs.
+ * Returns FA_OK if the kernel was launched.
+ */
+int fa_selftest_wait_timeout(void* stream);
+
+/* Human-readable name of an fa_status value (static string). */
+const char* fa_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

@@ -1,0 +1,111 @@
+"""The C-ABI library builds, loads without a GPU, exports every symbol that
+include/fa.h declares, and rejects bad arguments on the host before touching
+the device.  CPU only: no kernel is launched here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import exact_io_aware_06_gb300 as fa
+from exact_io_aware_06_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "fa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(fa_\w+)\s*\(", text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return fa.lib()
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("fa_fwd", "fa_fwd_fp8", "fa_bwd", "fa_bwd_workspace_size",
+                     "fa_last_device_error", "fa_status_string"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_only_declared_symbols_are_exported(L):
+    # hidden visibility: nothing but the C ABI leaks out of the library
+    out = os.popen(f"nm -D --defined-only {fa.LIB_PATH}").read()
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    assert {n for n in exported if n.startswith("fa_")} == set(declared_functions())
+
+
+def test_status_strings(L):
+    assert fa.fa_status_string(0) == "FA_OK"
+    assert fa.fa_status_string(1) == "FA_ERR_INVALID_ARG"
+    assert fa.fa_status_string(2) == "FA_ERR_UNSUPPORTED"
+    assert fa.fa_status_string(3) == "FA_ERR_CUDA"
+    assert fa.fa_status_string(4) == "FA_ERR_DEVICE_TIMEOUT"
+    assert fa.fa_status_string(99) == "FA_ERR_UNKNOWN"
+
+
+def test_workspace_size(L):
+    # delta + lse2 ([BH][Np]) and the fp32 dQ accumulator ([BH][Np][d]), Np = ceil128(N)
+    B, H, N, d = 4, 16, 2048, 64
+    assert fa.fa_bwd_workspace_size(B, H, N, d) == (2 * B * H * N + B * H * N * d) * 4
+    Np = 256
+    assert fa.fa_bwd_workspace_size(1, 3, 130, 64) == (2 * 3 * Np + 3 * Np * 64) * 4
+    assert fa.fa_bwd_workspace_size(0, 1, 1, 64) == 0
+    assert fa.fa_bwd_workspace_size(1, 1, 0, 64) == 0
+
+
+P = ctypes.c_void_p(0x10000)        # aligned, never dereferenced: rejected first
+MIS = ctypes.c_void_p(0x10008)      # misaligned
+
+
+def fwd(L, q=P, o=P, B=1, H=1, N=128, d=64, dtype=1, lse=None, scale=0.125):
+    return L.fa_fwd(q, P, P, o, lse, B, H, N, d, scale, 0, dtype, None)
+
+
+def test_fwd_argument_errors(L):
+    assert fwd(L, q=None) == 1
+    assert fwd(L, o=None) == 1
+    assert fwd(L, q=MIS) == 1
+    assert fwd(L, lse=MIS) == 1
+    assert fwd(L, N=0) == 1
+    assert fwd(L, B=0) == 1
+    assert fwd(L, H=-1) == 1
+    assert fwd(L, dtype=2) == 1          # E4M3 goes through fa_fwd_fp8
+    assert fwd(L, dtype=7) == 1
+    assert fwd(L, scale=float("nan")) == 1
+    assert fwd(L, d=96) == 2
+    assert fwd(L, d=256) == 2
+
+
+def test_fp8_argument_errors(L):
+    def f(qd=1.0, d=128, N=128):
+        return L.fa_fwd_fp8(P, P, P, P, None, qd, 1.0, 1.0, 1, 1, N, d, 0.1, 0, None)
+    assert f(qd=0.0) == 1
+    assert f(qd=-1.0) == 1
+    assert f(qd=float("inf")) == 1
+    assert f(N=0) == 1
+    assert f(d=64) == 2
+
+
+def test_bwd_argument_errors(L):
+    ws = fa.fa_bwd_workspace_size(1, 1, 128, 64)
+
+    def b(dtype=1, d=64, causal=0, ws_bytes=ws, dq=P, lse=P):
+        return L.fa_bwd(P, P, P, P, lse, P, dq, P, P, P, ws_bytes, 1, 1, 128, d, 0.125, causal,
+                        dtype, None)
+    assert b(dq=None) == 1
+    assert b(lse=None) == 1
+    assert b(ws_bytes=ws - 4) == 1
+    assert b(dtype=9) == 1
+    assert b(dtype=0) == 2
+    assert b(d=128) == 2
+    assert b(causal=1) == 2
