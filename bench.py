@@ -1,0 +1,418 @@
+"""Throughput of the exact-attention hot path on GB300 (TFLOP/s and % of peak).
+
+One step runs every stage of the path once, each on its own synthetic batch
+(iid N(0,1) inputs, seeds 42-45, scale 1/sqrt(d)):
+
+  fwd   bf16  B=1  H=32 N=16384 d=128  non-causal   (long-sequence forward)
+  fwd   bf16  B=1  H=32 N=16384 d=128  causal
+  fwd   bf16  B=4  H=16 N=1024  d=64   non-causal
+  fwd+bwd bf16 B=4 H=16 N=2048  d=64   non-causal   (forward, then delta / dK dV dQ / dQ convert)
+  fwd   e4m3  B=4  H=16 N=4096  d=128  non-causal   (per-tensor descales, bf16 O)
+
+FLOP counts: forward 4 B H N^2 d, backward 10 B H N^2 d, halved when causal.
+``value`` is the step's total FLOP over its device time (CUDA events on the
+launch stream, inputs resident in HBM); ``parts`` gives each stage alone.
+``e2e`` times the same step through the public API with pinned host buffers:
+inputs copied in and outputs copied out inside the timed region.
+
+``--impl reference`` times the fp64 CPU oracle instead (the comparison arm) on a
+bounded sample of the same workload, on this machine's host cores.
+
+Multi-GPU: the stages shard by head with no exchange, so N ranks run N
+independent replicas (weak scaling); rank 0 prints the line.
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fwd/bwd attention TFLOP/s on 1 GB300 and % of dense tensor-core peak"
+UNIT = "TFLOP/s"
+
+PARTS = [
+    # name, kind, dtype, B, H, N, d, causal
+    ("fwd_bf16_b1h32n16384d128", "fwd", "bf16", 1, 32, 16384, 128, False),
+    ("fwd_bf16_b1h32n16384d128_causal", "fwd", "bf16", 1, 32, 16384, 128, True),
+    ("fwd_bf16_b4h16n1024d64", "fwd", "bf16", 4, 16, 1024, 64, False),
+    ("fwdbwd_bf16_b4h16n2048d64", "fwdbwd", "bf16", 4, 16, 2048, 64, False),
+    ("fwd_e4m3_b4h16n4096d128", "fwd8", "e4m3", 4, 16, 4096, 128, False),
+]
+WORKLOAD = ("bf16 fwd B1 H32 N16384 d128 (non-causal + causal) + bf16 fwd B4 H16 N1024 d64 "
+            "+ bf16 fwd+bwd B4 H16 N2048 d64 + e4m3 fwd B4 H16 N4096 d128")
+LAUNCHES = {"fwd": 1, "fwd8": 1, "fwdbwd": 4}  # our kernels per part per step
+
+
+def flops(kind, B, H, N, d, causal):
+    f = {"fwd": 4, "fwd8": 4, "fwdbwd": 14}[kind] * B * H * N * N * d
+    return f / 2 if causal else f
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return {"bf16": p["bf16_tflops"], "bf16_sustained": p.get("bf16_tflops_sustained"),
+                "hbm_gbs": p["hbm_gbs"], "source": "measured"}
+    return {"bf16": 1900.0, "bf16_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = str(index)
+        try:  # address the GPU by UUID: robust to CUDA_VISIBLE_DEVICES remapping
+            import torch
+            self.index = "GPU-" + str(torch.cuda.get_device_properties(index).uuid)
+        except Exception:  # noqa: BLE001
+            pass
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.index, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for ln in (self.out or "").splitlines():
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[4:8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for _, _, flags in rows for n, f in zip(names, flags)
+                          if f.lower() == "active"})
+        loaded = [r[0] for r in rows]
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- our arm
+_INPUT_CACHE = {}
+
+
+def make_part(torch, fa, inputs, part, dev):
+    name, kind, dt, B, H, N, d, causal = part
+    key = (kind, dt, B, H, N, d)
+    if key not in _INPUT_CACHE:  # parts with equal shapes share one input batch
+        x = inputs.attention_inputs(B, H, N, d, dt, with_do=(kind == "fwdbwd"))
+        host = {n: t.pin_memory() for n, t in x.items() if torch.is_tensor(t)}
+        _INPUT_CACHE[key] = (x, host, {n: t.to(dev) for n, t in host.items()})
+    x, host, dev_in = _INPUT_CACHE[key]
+    P = {"part": part, "host": host, "scale": 1.0 / math.sqrt(d), "dev": dev_in}
+    out_dtype = torch.bfloat16
+    P["o"] = torch.empty((B, H, N, d), dtype=out_dtype, device=dev)
+    P["lse"] = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    outs = {"o": P["o"]}
+    if kind == "fwd8":
+        P["descales"] = (x["q_descale"], x["k_descale"], x["v_descale"])
+    if kind == "fwdbwd":
+        P["ws"] = torch.empty(fa.fa_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
+        for g in ("dq", "dk", "dv"):
+            P[g] = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev)
+            outs[g] = P[g]
+    P["outs"] = outs
+    P["host_out"] = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory() for n, t in outs.items()}
+    P["flop"] = flops(kind, B, H, N, d, causal)
+    P["h2d"] = sum(t.numel() * t.element_size() for t in host.values())
+    P["d2h"] = sum(t.numel() * t.element_size() for t in outs.values())
+    return P
+
+
+def run_part(fa, P, stream):
+    name, kind, dt, B, H, N, d, causal = P["part"]
+    D = P["dev"]
+    if kind == "fwd8":
+        qd, kd, vd = P["descales"]
+        fa.fa_fwd_fp8(D["q"], D["k"], D["v"], P["o"], P["lse"], qd, kd, vd, P["scale"], causal,
+                      stream)
+    else:
+        fa.fa_fwd(D["q"], D["k"], D["v"], P["o"], P["lse"], P["scale"], causal, fa.FA_BF16, stream)
+    if kind == "fwdbwd":
+        fa.fa_bwd(D["q"], D["k"], D["v"], P["o"], P["lse"], D["do"], P["dq"], P["dk"], P["dv"],
+                  P["ws"], P["scale"], False, fa.FA_BF16, stream)
+
+
+def run_part_e2e(fa, P, stream):
+    for n, t in P["host"].items():
+        P["dev"][n].copy_(t, non_blocking=True)
+    run_part(fa, P, stream)
+    for n, t in P["outs"].items():
+        P["host_out"][n].copy_(t, non_blocking=True)
+
+
+def fp8_peak(torch, dev):
+    """Dense e4m3 GEMM throughput (torch._scaled_mm, 8192^3, best of 10)."""
+    try:
+        n = 8192
+        a = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn)
+        b = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn).t()
+        one = torch.tensor(1.0, device=dev)
+        for _ in range(3):
+            torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        best = float("inf")
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+            e1.record()
+            e1.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        return 2 * n ** 3 / (best * 1e-3) / 1e12, "measured: torch._scaled_mm e4m3 8192^3 best of 10"
+    except Exception as ex:  # noqa: BLE001 - report and fall back
+        return None, f"unmeasured ({type(ex).__name__})"
+
+
+def cpu_sample(oracle, inputs, budget_s):
+    """Time the fp64 oracle on a bounded sample of the step's workload.
+    Returns (metric FLOP of the sample, seconds, description)."""
+    import numpy as np
+    f64 = lambda t: t.float().numpy().astype(np.float64)
+    units = []
+    # rows of the long-sequence forward (non-causal and causal), one head each
+    big = inputs.attention_inputs(1, 1, 16384, 128, "bf16")
+    qb, kb, vb = f64(big["q"][0, 0]), f64(big["k"][0, 0]), f64(big["v"][0, 0])
+    rng = np.random.default_rng(0)
+    for causal in (False, True):
+        rows = np.sort(rng.choice(16384, 32, replace=False))
+        fl = sum(4 * ((r + 1) if causal else 16384) * 128 for r in rows)
+        units.append((lambda rows=rows, c=causal: oracle.attn_fwd_rows(
+            qb, kb, vb, rows, 1 / math.sqrt(128), c), fl))
+    # one head of the fwd+bwd workload
+    m = inputs.attention_inputs(1, 1, 2048, 64, "bf16", with_do=True)
+    qm, km, vm, dm = (f64(m[n][0, 0]) for n in ("q", "k", "v", "do"))
+    units.append((lambda: (oracle.attn_fwd(qm, km, vm, 1 / 8.0),
+                           oracle.attn_bwd(qm, km, vm, dm, 1 / 8.0)), 14 * 2048 * 2048 * 64))
+    # rows of the e4m3 forward on dequantised inputs
+    e = inputs.attention_inputs(1, 1, 4096, 128, "e4m3")
+    qe = oracle.e4m3_decode(e["q"][0, 0].numpy(), e["q_descale"])
+    ke = oracle.e4m3_decode(e["k"][0, 0].numpy(), e["k_descale"])
+    ve = oracle.e4m3_decode(e["v"][0, 0].numpy(), e["v_descale"])
+    rows8 = np.arange(0, 4096, 64)
+    units.append((lambda: oracle.attn_fwd_rows(qe, ke, ve, rows8, 1 / math.sqrt(128)),
+                  4 * len(rows8) * 4096 * 128))
+    total_f, reps = 0.0, 0
+    t0 = time.perf_counter()
+    while True:
+        for fn, fl in units:
+            fn()
+            total_f += fl
+        reps += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    desc = (f"{reps} x [32 rows non-causal + 32 rows causal of one N=16384 d=128 head, one "
+            f"N=2048 d=64 head fwd+bwd, 64 rows of one N=4096 d=128 e4m3 head]")
+    return total_f, dt, desc
+
+
+def bench_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import exact_io_aware_06_gb300 as fa
+    from exact_io_aware_06_gb300 import inputs
+
+    stream = torch.cuda.current_stream()
+    parts = [make_part(torch, fa, inputs, p, dev) for p in PARTS]
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def step_timed(events):
+        for i, P in enumerate(parts):
+            events[i].record(stream)
+            run_part(fa, P, stream)
+        events[-1].record(stream)
+
+    for _ in range(args.warmup):
+        for P in parts:
+            run_part(fa, P, stream)
+    st = fa.fa_last_device_error()
+    if st != 0:
+        raise RuntimeError(f"device status {fa.fa_status_string(st)}")
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(parts) + 1)] for _ in range(K)]
+    barrier()
+    with ClockSampler(local) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for k in range(K):
+            step_timed(evs[k])
+        t_end.record(stream)
+        barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    st = fa.fa_last_device_error()
+    if st != 0:
+        raise RuntimeError(f"device status {fa.fa_status_string(st)}")
+    part_ms = [[evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(K)] for i in range(len(parts))]
+
+    # e2e: same step with pinned host buffers, copies inside the timed region
+    Ke = max(3, K // 10)
+    for P in parts:
+        run_part_e2e(fa, P, stream)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(Ke):
+        for P in parts:
+            run_part_e2e(fa, P, stream)
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / Ke
+
+    ms_step = total_ms / K
+    if world > 1:
+        t = torch.tensor([ms_step, e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step, e2e_ms = float(t[0]), float(t[1])
+    step_flop = sum(P["flop"] for P in parts)
+    value = world * step_flop / (ms_step * 1e-3) / 1e12
+    pk = peaks()
+    fp8_tf, fp8_how = fp8_peak(torch, dev)
+
+    part_out = {}
+    for P, ms in zip(parts, part_ms):
+        name, kind, dt = P["part"][0], P["part"][1], P["part"][2]
+        mean = sum(ms) / len(ms)
+        tf = P["flop"] / (mean * 1e-3) / 1e12
+        peak = (fp8_tf or 2 * pk["bf16"]) if dt == "e4m3" else pk["bf16"]
+        part_out[name] = {"ms": round(mean, 4), "best_ms": round(min(ms), 4),
+                          "tflops": round(tf, 1), "pct_of_peak": round(100 * tf / peak, 1),
+                          "peak_tflops": round(peak, 1), "flop": P["flop"]}
+
+    dom = part_out[PARTS[0][0]]
+    roofline = {"kernel": "fwd_sm103_kernel<128,bf16> (B1 H32 N16384 d128 non-causal)",
+                "bound": "tensor", "achieved": dom["tflops"], "peak": pk["bf16"],
+                "unit": "TFLOP/s", "frac": round(dom["tflops"] / pk["bf16"], 4),
+                "peak_source": f"{pk['source']} bf16 burst (sustained {pk['bf16_sustained']})",
+                "traffic": args.traffic}
+
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "inputs larger than L2: each part follows a part that streams >129 MB"},
+        "pct_of_peak": round(100 * value / world / pk["bf16"], 1),
+        "parts": part_out,
+        "fp8_peak_tflops": None if fp8_tf is None else round(fp8_tf, 1), "fp8_peak_how": fp8_how,
+        "roofline": roofline,
+        "e2e": {"value": round(world * step_flop / (e2e_ms * 1e-3) / 1e12, 1), "unit": UNIT,
+                "ms_per_step": round(e2e_ms, 3),
+                "h2d_bytes_per_step": sum(P["h2d"] for P in parts),
+                "d2h_bytes_per_step": sum(P["d2h"] for P in parts)},
+        "gpu_launches": K * sum(LAUNCHES[P["part"][1]] for P in parts),
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu:
+        import oracle
+        fl, dt, desc = cpu_sample(oracle, inputs, args.cpu_seconds)
+        result["cpu_baseline"] = {"value": round(fl / dt / 1e12, 6), "unit": UNIT,
+                                  "cores": oracle.max_threads(), "kind": "oracle",
+                                  "sample": desc, "seconds": round(dt, 2)}
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+# ---------------------------------------------------------------- reference arm
+def bench_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    from exact_io_aware_06_gb300 import inputs
+    for _ in range(args.warmup):
+        cpu_sample(oracle, inputs, 0.0)
+    total_f, total_t = 0.0, 0.0
+    desc = None
+    for _ in range(args.steps):
+        fl, dt, desc = cpu_sample(oracle, inputs, 0.0)
+        total_f += fl
+        total_t += dt
+    value = total_f / total_t / 1e12
+    cores = oracle.max_threads()
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * total_t / args.steps, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "parallelism": "single"},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": "each step: " + desc},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per launch of the dominant kernel from an ncu capture")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        bench_reference(args)
+    else:
+        bench_ours(args)
+
+
+if __name__ == "__main__":
+    main()
