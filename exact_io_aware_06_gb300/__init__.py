@@ -15,7 +15,7 @@ import os
 
 __all__ = [
     "FaError", "FA_F32", "FA_BF16", "FA_E4M3", "lib", "fa_fwd", "fa_fwd_fp8", "fa_bwd",
-    "fa_bwd_workspace_size", "fa_last_device_error", "fa_set_wait_timeout_ns",
+    "fa_bwd_workspace_size", "fa_bwd_noalloc", "fa_last_device_error", "fa_set_wait_timeout_ns",
     "fa_selftest_wait_timeout", "fa_status_string", "attention_forward", "attention_backward",
 ]
 
@@ -51,6 +51,8 @@ def lib():
         L.fa_bwd_workspace_size.restype = sz
         L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, f, i, i, vp]
         L.fa_bwd.restype = i
+        L.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
+        L.fa_bwd_noalloc.restype = i
         L.fa_last_device_error.argtypes = [vp]
         L.fa_last_device_error.restype = i
         L.fa_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
@@ -120,6 +122,16 @@ def fa_bwd(q, k, v, o, lse, do, dq, dk, dv, workspace, scale, causal, dtype, str
     _check(lib().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq),
                         _ptr(dk), _ptr(dv), _ptr(workspace), nbytes, B, H, N, d, float(scale),
                         int(bool(causal)), int(dtype), _stream(stream)), "fa_bwd")
+
+
+def fa_bwd_noalloc(q, k, v, o, lse, do, dq, dk, dv, scale, causal, dtype, stream=None):
+    """fa_bwd with the library's built-in scratch (no workspace, no allocation).
+    For callers that cannot allocate device memory at call time; calls that
+    overlap on the GPU race on the shared scratch."""
+    B, H, N, d = _shape(q)
+    _check(lib().fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),
+                                _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, float(scale),
+                                int(bool(causal)), int(dtype), _stream(stream)), "fa_bwd_noalloc")
 
 
 def fa_last_device_error(stream=None):

@@ -125,6 +125,34 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
            int dtype, void* stream);
 
 /*
+ * fa_bwd without a caller-supplied workspace, for callers that cannot allocate
+ * device memory when they run the backward -- for example a plug-in called
+ * from a host framework that owns the device memory budget and forbids
+ * allocation inside its execution hook, or a latency-critical caller that
+ * cannot afford cudaMalloc's implicit device synchronisation.  The pages have
+ * no counterpart to this entry point; it is a deployment convenience.
+ *
+ * Arguments and results are those of fa_bwd minus (workspace,
+ * workspace_bytes).  The scratch is a fixed 64 MiB array inside the library
+ * (a file-scope __device__ array that every GPU loading the library holds until
+ * the process exits); the call allocates nothing.  Sizes whose
+ * fa_bwd_workspace_size() exceeds 64 MiB are refused with FA_ERR_UNSUPPORTED
+ * before anything is launched (at d = 64 that allows B*H*ceil128(N) up to
+ * 254,200 rows, e.g. B=4, H=16, N=2048).
+ *
+ * The first call on a device looks up the array's device address for that
+ * device (with that device current); make that first call before any stream
+ * capture.  All calls on a device share the one array and it keeps the last
+ * call's contents: each call writes every scratch region it reads before
+ * reading it, so nothing carries over, but calls that overlap in time on the
+ * GPU (different streams, or other host threads) race on the array and give
+ * wrong results.  FA_ERR_CUDA if the address lookup fails.
+ */
+int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                   const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                   float scale, int causal, int dtype, void* stream);
+
+/*
  * Synchronise `stream`, then return and clear the current device's status
  * word: FA_OK, or the first device-side error recorded since the last call
  * (FA_ERR_DEVICE_TIMEOUT when a kernel's bounded wait ran out; that kernel
