@@ -95,25 +95,68 @@ __device__ __forceinline__ void record_timeout(const DevCtl& ctl, volatile int* 
     atomicCAS(ctl.status, kDevOk, kDevTimeout);
 }
 
-// Keep the compiler from using TMEM-load results before the wait instruction.
-__device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
-#pragma unroll
-    for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(r[i]));
-}
-
-__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t (&r)[32]) {
+// 32 consecutive TMEM columns of this thread's lane into r[OFF..OFF+31], no wait.
+template <int OFF>
+__device__ __forceinline__ void tmem_ld32_at(uint32_t taddr, uint32_t (&r)[128]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
         "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
         "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-          "=r"(r[31])
+        : "=r"(r[OFF + 0]), "=r"(r[OFF + 1]), "=r"(r[OFF + 2]), "=r"(r[OFF + 3]),
+          "=r"(r[OFF + 4]), "=r"(r[OFF + 5]), "=r"(r[OFF + 6]), "=r"(r[OFF + 7]),
+          "=r"(r[OFF + 8]), "=r"(r[OFF + 9]), "=r"(r[OFF + 10]), "=r"(r[OFF + 11]),
+          "=r"(r[OFF + 12]), "=r"(r[OFF + 13]), "=r"(r[OFF + 14]), "=r"(r[OFF + 15]),
+          "=r"(r[OFF + 16]), "=r"(r[OFF + 17]), "=r"(r[OFF + 18]), "=r"(r[OFF + 19]),
+          "=r"(r[OFF + 20]), "=r"(r[OFF + 21]), "=r"(r[OFF + 22]), "=r"(r[OFF + 23]),
+          "=r"(r[OFF + 24]), "=r"(r[OFF + 25]), "=r"(r[OFF + 26]), "=r"(r[OFF + 27]),
+          "=r"(r[OFF + 28]), "=r"(r[OFF + 29]), "=r"(r[OFF + 30]), "=r"(r[OFF + 31])
         : "r"(taddr)
         : "memory");
+}
+
+// Wait for this thread's outstanding TMEM loads, then route every loaded register
+// through an empty asm so no use of them can be scheduled before the wait.
+__device__ __forceinline__ void tmem_wait_ld_fence(uint32_t (&r)[128]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 128; ++i) asm volatile("" : "+r"(r[i]));
+}
+
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+__device__ __forceinline__ float min3f(float a, float b, float c) {
+    float d;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Max (or, for a negative score scale, min) of the 128 raw scores: four
+// independent 3-input chains over r[4..123], then r[124..127].
+__device__ __forceinline__ float block_extreme(const uint32_t (&r)[128], bool want_max) {
+    float a[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) a[k] = __uint_as_float(r[k]);
+    if (want_max) {
+#pragma unroll
+        for (int i = 4; i < 124; i += 8)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                a[k] = max3f(a[k], __uint_as_float(r[i + 2 * k]), __uint_as_float(r[i + 2 * k + 1]));
+        a[0] = max3f(a[0], __uint_as_float(r[124]), __uint_as_float(r[125]));
+        a[1] = max3f(a[1], __uint_as_float(r[126]), __uint_as_float(r[127]));
+        return max3f(a[0], a[1], fmaxf(a[2], a[3]));
+    }
+#pragma unroll
+    for (int i = 4; i < 124; i += 8)
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            a[k] = min3f(a[k], __uint_as_float(r[i + 2 * k]), __uint_as_float(r[i + 2 * k + 1]));
+    a[0] = min3f(a[0], __uint_as_float(r[124]), __uint_as_float(r[125]));
+    a[1] = min3f(a[1], __uint_as_float(r[126]), __uint_as_float(r[127]));
+    return min3f(a[0], a[1], fminf(a[2], a[3]));
 }
 
 template <int D, bool FP8>
@@ -170,6 +213,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = tmem_slot;
     const uint64_t lim = args.ctl.wait_ns;
 
+    // 384 threads x 168 registers at launch: warpgroup 0 (load, MMA) gives up to
+    // 120 per thread, the two softmax warpgroups take 184 (128*120 + 256*184 <= 384*168).
+    if (warp < 4) {
+    regs_dec<120>();
     if (warp == 0) {
         // ================================================================ TMA producer
         if (lane == 0) {
@@ -294,7 +341,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const volatile int never = 0;
             mbar_wait(smem_u32(&bars.drain), 0, kDrainWaitNs, &never);
         }
-    } else if (warp >= 4) {
+    }
+    // warps 2-3 have no role
+    } else {
+        regs_inc<184>();
         // ================================================================ softmax warpgroups
         const int t = (warp - 4) / 4;              // query tile 0 or 1
         const int wq = warp % 4;                   // TMEM lane quarter
@@ -304,6 +354,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t colS = t ? C::kColS1 : C::kColS0;
         const uint32_t colO = t ? C::kColO1 : C::kColO0;
         const float c = args.c_log2;
+        const bool c_pos = c >= 0.f;
+        // a masked score must become -inf after the multiply by c
+        const uint32_t mask_bits = c_pos ? 0xff800000u : 0x7f800000u;
         float m_ref = -INFINITY;  // reference max in log2 units
         float l = 0.f;
         bool ok = true;
@@ -313,32 +366,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            uint32_t r[4][32];
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) tmem_ld32_nowait(lane_base + colS + 32 * q4, r[q4]);
-            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) reg_fence(r[q4]);
+            uint32_t r[128];
+            tmem_ld32_at<0>(lane_base + colS, r);
+            tmem_ld32_at<32>(lane_base + colS + 32, r);
+            tmem_ld32_at<64>(lane_base + colS + 64, r);
+            tmem_ld32_at<96>(lane_base + colS + 96, r);
+            tmem_wait_ld_fence(r);
 
-            float x[128];
             const int kv0 = j * kBN;
-            const bool need_mask = (kv0 + kBN > N) || (args.causal && kv0 + kBN - 1 > qrow);
-            float mt = -INFINITY;
-            if (need_mask) {
+            if ((kv0 + kBN > N) || (args.causal && kv0 + kBN - 1 > qrow)) {
+                // keys >= N, and keys after this query row when causal, drop out
+                const int valid = min(N - kv0, args.causal ? qrow - kv0 + 1 : kBN);
 #pragma unroll
-                for (int i = 0; i < 128; ++i) {
-                    const int key = kv0 + i;
-                    const bool masked = key >= N || (args.causal && key > qrow);
-                    x[i] = masked ? -INFINITY : __uint_as_float(r[i / 32][i % 32]) * c;
-                    mt = fmaxf(mt, x[i]);
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 128; ++i) {
-                    x[i] = __uint_as_float(r[i / 32][i % 32]) * c;
-                    mt = fmaxf(mt, x[i]);
-                }
+                for (int i = 0; i < 128; ++i)
+                    if (i >= valid) r[i] = mask_bits;
             }
+            // block max of the scaled scores = c * (max of the raw scores) for c >= 0
+            const float mt = c * block_extreme(r, c_pos);
             // lazy rescale: move the reference only when the block max exceeds it by > kTau
             float alpha = 1.f;
             const bool bump = mt > m_ref + kTau;
@@ -347,9 +391,46 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_ref = mt;
                 l *= alpha;
             }
+            const float ref = (m_ref == -INFINITY) ? 0.f : m_ref;
+            const float2 c2 = make_float2(c, c), nref2 = make_float2(-ref, -ref);
+            float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0;
+            if (FP8) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float2 x01 = __ffma2_rn(
+                        make_float2(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1])), c2, nref2);
+                    const float2 x23 = __ffma2_rn(
+                        make_float2(__uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])), c2, nref2);
+                    const float2 p01 = make_float2(ex2_approx(x01.x), ex2_approx(x01.y));
+                    const float2 p23 = make_float2(ex2_approx(x23.x), ex2_approx(x23.y));
+                    acc0 = __fadd2_rn(acc0, p01);
+                    acc1 = __fadd2_rn(acc1, p23);
+                    pk[i] = pack_e4m3x4(p01.x, p01.y, p23.x, p23.y);
+                }
+                tmem_st32(lane_base + colS, pk);
+            } else {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int e = 64 * h + 2 * i;
+                        const float2 x = __ffma2_rn(
+                            make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), c2, nref2);
+                        const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                        if (i & 1)
+                            acc1 = __fadd2_rn(acc1, p);
+                        else
+                            acc0 = __fadd2_rn(acc0, p);
+                        pk[i] = pack_bf16x2(p.x, p.y);
+                    }
+                    tmem_st32(lane_base + colS + 32 * h, pk);
+                }
+            }
             if (j > 0 && __any_sync(0xffffffffu, bump)) {
                 // O_t += P V of the previous block has completed (it precedes S_t(j) in
-                // issue order), so O_t can be rescaled in place.
+                // issue order), so O_t can be rescaled in place before P_t(j) is published.
 #pragma unroll
                 for (int q4 = 0; q4 < D / 32; ++q4) {
                     uint32_t ov[32];
@@ -359,32 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_st32(lane_base + colO + 32 * q4, ov);
                 }
             }
-            const float ref = (m_ref == -INFINITY) ? 0.f : m_ref;
-            float rs = 0.f;
-            if (FP8) {
-                uint32_t pk[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float p0 = ex2_approx(x[4 * i] - ref), p1 = ex2_approx(x[4 * i + 1] - ref);
-                    const float p2 = ex2_approx(x[4 * i + 2] - ref), p3 = ex2_approx(x[4 * i + 3] - ref);
-                    rs += (p0 + p1) + (p2 + p3);
-                    pk[i] = pack_e4m3x4(p0, p1, p2, p3);
-                }
-                tmem_st32(lane_base + colS, pk);
-            } else {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const float p0 = ex2_approx(x[64 * h + 2 * i] - ref);
-                        const float p1 = ex2_approx(x[64 * h + 2 * i + 1] - ref);
-                        rs += p0 + p1;
-                        pk[i] = pack_bf16x2(p0, p1);
-                    }
-                    tmem_st32(lane_base + colS + 32 * h, pk);
-                }
-            }
+            const float rs = (acc0.x + acc0.y) + (acc1.x + acc1.y);
             l += rs;
             tmem_st_wait();
             tc_fence_before();
@@ -420,7 +476,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 args.lse[static_cast<size_t>(bh) * N + qrow] = (m_ref + log2f(l)) * 0.69314718055994530942f;
         }
     }
-    // warps 2-3 have no role
 
     tc_fence_before();
     __syncthreads();

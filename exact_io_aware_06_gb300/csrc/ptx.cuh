@@ -262,6 +262,19 @@ __device__ __forceinline__ void tmem_st_wait() {
 #undef FA_R8
 #undef FA_W8
 
+// ------------------------------------------------------------------ register budget
+// Change this warpgroup's per-thread register allotment (all 128 threads of the
+// warpgroup must execute it).  The block's total is fixed at launch, so the
+// increases and decreases across warpgroups must balance.
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ------------------------------------------------------------------ math / packing
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
