@@ -17,19 +17,22 @@
 //                    accumulator with vector atomics.
 //   3. bwd_dq_convert  dQ = bf16(scale * accumulator).
 //
-// bwd_main layout (d = 64):
-//   warp 0      TMA producer: K_j, V_j once; Q_i, dO_i, lse_i, delta_i in a 2-stage ring
+// bwd_main layout (d = 64), 16 warps:
+//   warp 0      TMA producer: K_j, V_j once; Q_i, dO_i, lse_i, delta_i in a 3-stage ring
 //   warp 1      MMA issuer + TMEM owner
-//   warps 4-7   "P/dS" warpgroup: thread = key row of the block
-//   warps 8-11  "dQ" warpgroup: drains dQ_i from TMEM into the accumulator
-//   TMEM: S^T 0-127 (P^T bf16 over 0-63), dP^T 128-255 (dS^T bf16 over 128-191),
+//   warps 4-7   P/dS for query columns 0-63 of block i   (thread = key row)
+//   warps 8-11  P/dS for query columns 64-127
+//   warps 12-15 drain dQ_i from TMEM into the fp32 accumulator (vector atomics)
+//   TMEM: S^T 0-127 (P^T bf16 over 0-31 and 64-95), dP^T 128-255 (dS^T bf16 over
+//         128-159 and 192-223: each half writes only inside the columns it read),
 //         dV 256-319, dK 320-383, dQ double buffer 384-447 / 448-511.
-//   MMAs per query block i (M = 128 keys or queries):
-//     S^T  = K_j Q_i^T        (SS, both K-major)
-//     dP^T = V_j dO_i^T       (SS, both K-major)
-//     dV  += P^T dO_i         (TS, dO_i MN-major)
-//     dK  += dS^T Q_i         (TS, Q_i MN-major)
-//     dQ_i = dS K_j           (SS, dS from shared memory MN-major, K_j MN-major)
+//   MMAs per query block i (M = 128 keys or queries), in issue order:
+//     dV  += P^T dO_i         (TS, dO_i MN-major)          after P_i is in TMEM
+//     S^T  = K_j Q_{i+1}^T    (SS, both K-major)           P_i lives on in registers
+//     dK  += dS^T Q_i         (TS, Q_i MN-major)           after dS_i is in TMEM/smem
+//     dP^T = V_j dO_{i+1}^T   (SS, both K-major)
+//     dQ_i = dS_i K_j         (SS, dS from smem MN-major, K_j MN-major)
+//   so the next block's scores are ready when the P/dS warps finish dS_i.
 #include <cmath>
 
 #include "internal.h"
@@ -41,20 +44,21 @@ namespace {
 
 constexpr int kD = 64;
 constexpr int kBlk = 128;            // keys per CTA, queries per inner step
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
+constexpr int kQStages = 3;
 constexpr int kTile = kBlk * kD * 2;  // 16 KB bf16 tile (one 128-byte swizzle column)
 constexpr float kLog2e = 1.4426950408889634f;
 
 // shared memory map (offsets from a 1 KB aligned base)
 constexpr int kOffK = 0;
 constexpr int kOffV = kOffK + kTile;
-constexpr int kOffQ = kOffV + kTile;             // 2 stages
-constexpr int kOffDO = kOffQ + 2 * kTile;        // 2 stages
-constexpr int kOffDS = kOffDO + 2 * kTile;       // 2 buffers x 32 KB (two 64-query columns)
+constexpr int kOffQ = kOffV + kTile;                     // kQStages
+constexpr int kOffDO = kOffQ + kQStages * kTile;         // kQStages
+constexpr int kOffDS = kOffDO + kQStages * kTile;        // 2 buffers x 32 KB (two 64-query columns)
 constexpr int kDSBytes = kBlk * kBlk * 2;
-constexpr int kOffL = kOffDS + 2 * kDSBytes;     // 2 stages x 512 B
-constexpr int kOffDelta = kOffL + 2 * kBlk * 4;  // 2 stages x 512 B
-constexpr int kSmemBytes = kOffDelta + 2 * kBlk * 4;
+constexpr int kOffL = kOffDS + 2 * kDSBytes;             // kQStages x 512 B
+constexpr int kOffDelta = kOffL + kQStages * kBlk * 4;   // kQStages x 512 B
+constexpr int kSmemBytes = kOffDelta + kQStages * kBlk * 4;
 constexpr int kSmemAlloc = kSmemBytes + 1024;
 
 constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 320, kColDQ = 384;
@@ -64,8 +68,8 @@ constexpr uint32_t kIdescTS = idesc_bf16(128, kD, false, true);    // dV, dK
 constexpr uint32_t kIdescDQ = idesc_bf16(128, kD, true, true);     // dQ (A MN-major)
 
 struct BwdArgs {
-    const float* ws_delta;  // [BH][Np]
-    const float* ws_lse2;   // [BH][Np]
+    const float* ws_delta;  // [BH][Np], negated: -delta_i
+    const float* ws_lse2;   // [BH][Np], negated: -lse_i * log2(e)
     float* dq_acc;          // [BH][Np][d]
     void* dk;
     void* dv;
@@ -77,7 +81,7 @@ struct BwdArgs {
 
 struct Bars {
     uint64_t kv_full;
-    uint64_t q_full[2], q_empty[2];
+    uint64_t q_full[kQStages], q_empty[kQStages];
     uint64_t s_full, dp_full, p_full, ds_full;
     uint64_t ds_empty[2];
     uint64_t dq_full[2], dq_free[2];
@@ -111,17 +115,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         abort_flag = 0;
         mbar_init(smem_u32(&bars.kv_full), 1);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < kQStages; ++s) {
             mbar_init(smem_u32(&bars.q_full[s]), 1);
             mbar_init(smem_u32(&bars.q_empty[s]), 1);
+        }
+        for (int s = 0; s < 2; ++s) {
             mbar_init(smem_u32(&bars.ds_empty[s]), 1);
             mbar_init(smem_u32(&bars.dq_full[s]), 1);
             mbar_init(smem_u32(&bars.dq_free[s]), 128);
         }
         mbar_init(smem_u32(&bars.s_full), 1);
         mbar_init(smem_u32(&bars.dp_full), 1);
-        mbar_init(smem_u32(&bars.p_full), 128);
-        mbar_init(smem_u32(&bars.ds_full), 128);
+        mbar_init(smem_u32(&bars.p_full), 256);
+        mbar_init(smem_u32(&bars.ds_full), 256);
         mbar_init(smem_u32(&bars.all_done), 1);
         mbar_init(smem_u32(&bars.drain), 1);
         fence_barrier_init();
@@ -151,8 +157,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             int issued = 0;
             bool ok = true;
             for (int i = 0; i < n_q; ++i) {
-                const int s = i & 1;
-                if (i >= 2 && !mbar_wait(smem_u32(&bars.q_empty[s]), ((i >> 1) & 1) ^ 1, lim, &abort_flag)) {
+                const int s = i % kQStages;
+                if (i >= kQStages &&
+                    !mbar_wait(smem_u32(&bars.q_empty[s]), ((i / kQStages) & 1) ^ 1, lim, &abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -168,35 +175,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) record_timeout(args.ctl, &abort_flag);
             const volatile int never = 0;
             mbar_wait(kvf, 0, kDrainWaitNs, &never);
-            for (int i = max(0, issued - 2); i < issued; ++i)
-                mbar_wait(smem_u32(&bars.q_full[i & 1]), (i >> 1) & 1, kDrainWaitNs, &never);
+            for (int i = max(0, issued - kQStages); i < issued; ++i)
+                mbar_wait(smem_u32(&bars.q_full[i % kQStages]), (i / kQStages) & 1, kDrainWaitNs,
+                          &never);
         }
     } else if (warp == 1) {
         // ================================================================ MMA issuer
         if (lane == 0) {
             const uint32_t sK = sb + kOffK, sV = sb + kOffV;
-            bool ok = mbar_wait(smem_u32(&bars.kv_full), 0, lim, &abort_flag);
-            // S^T = K_j Q_i^T and dP^T = V_j dO_i^T for query block i (stage s)
-            auto issue_s_dp = [&](int s) {
-                const uint32_t sQ = sb + kOffQ + s * kTile, sDO = sb + kOffDO + s * kTile;
+            auto issue_s = [&](int s) {  // S^T = K_j Q^T into columns 0-127
+                const uint32_t sQ = sb + kOffQ + s * kTile;
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk)
                     mma_bf16_ss(tmem + kColS, sdesc_sw128(sK + 32 * kk, 16, 1024),
                                 sdesc_sw128(sQ + 32 * kk, 16, 1024), kIdescSS, kk > 0);
                 mma_commit(smem_u32(&bars.s_full));
+            };
+            auto issue_dp = [&](int s) {  // dP^T = V_j dO^T into columns 128-255
+                const uint32_t sDO = sb + kOffDO + s * kTile;
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk)
                     mma_bf16_ss(tmem + kColDP, sdesc_sw128(sV + 32 * kk, 16, 1024),
                                 sdesc_sw128(sDO + 32 * kk, 16, 1024), kIdescSS, kk > 0);
                 mma_commit(smem_u32(&bars.dp_full));
             };
+            bool ok = mbar_wait(smem_u32(&bars.kv_full), 0, lim, &abort_flag);
             if (ok) ok = mbar_wait(smem_u32(&bars.q_full[0]), 0, lim, &abort_flag);
             if (ok) {
                 tc_fence_after();
-                issue_s_dp(0);
+                issue_s(0);
+                issue_dp(0);
             }
             for (int i = 0; i < n_q && ok; ++i) {
-                const int s = i & 1;
+                const int s = i % kQStages;
+                const int s1 = (i + 1) % kQStages;
+                const bool more = i + 1 < n_q;
                 const uint32_t sQ = sb + kOffQ + s * kTile, sDO = sb + kOffDO + s * kTile;
                 // dV += P^T dO_i
                 ok = mbar_wait(smem_u32(&bars.p_full), i & 1, lim, &abort_flag);
@@ -204,37 +217,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < kBlk / 16; ++kk)
-                    mma_bf16_ts(tmem + kColDV, tmem + kColS + 8 * kk,
+                    mma_bf16_ts(tmem + kColDV, tmem + kColS + 64 * (kk >> 2) + 8 * (kk & 3),
                                 sdesc_sw128(sDO + 2048 * kk, 16384, 1024), kIdescTS, (i > 0) || (kk > 0));
+                // next block's scores: the P/dS warps keep P_i in registers
+                if (more) {
+                    ok = mbar_wait(smem_u32(&bars.q_full[s1]), ((i + 1) / kQStages) & 1, lim, &abort_flag);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_s(s1);
+                }
                 // dK += dS^T Q_i
                 ok = mbar_wait(smem_u32(&bars.ds_full), i & 1, lim, &abort_flag);
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < kBlk / 16; ++kk)
-                    mma_bf16_ts(tmem + kColDK, tmem + kColDP + 8 * kk,
+                    mma_bf16_ts(tmem + kColDK, tmem + kColDP + 64 * (kk >> 2) + 8 * (kk & 3),
                                 sdesc_sw128(sQ + 2048 * kk, 16384, 1024), kIdescTS, (i > 0) || (kk > 0));
                 mma_commit(smem_u32(&bars.q_empty[s]));  // Q_i, dO_i, lse_i, delta_i consumed
-                // next block's S^T and dP^T overlap with this block's dQ
-                if (i + 1 < n_q) {
-                    ok = mbar_wait(smem_u32(&bars.q_full[s ^ 1]), ((i + 1) >> 1) & 1, lim, &abort_flag);
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_s_dp(s ^ 1);
-                }
-                // dQ_i = dS_i K_j into TMEM buffer s
+                if (more) issue_dp(s1);
+                // dQ_i = dS_i K_j into TMEM buffer i % 2
+                const int b = i & 1;
                 if (i >= 2) {
-                    ok = mbar_wait(smem_u32(&bars.dq_free[s]), ((i >> 1) & 1) ^ 1, lim, &abort_flag);
+                    ok = mbar_wait(smem_u32(&bars.dq_free[b]), ((i >> 1) & 1) ^ 1, lim, &abort_flag);
                     if (!ok) break;
                     tc_fence_after();
                 }
-                const uint32_t sDS = sb + kOffDS + s * kDSBytes;
+                const uint32_t sDS = sb + kOffDS + b * kDSBytes;
 #pragma unroll
                 for (int kk = 0; kk < kBlk / 16; ++kk)
-                    mma_bf16_ss(tmem + kColDQ + 64 * s, sdesc_sw128(sDS + 2048 * kk, 16384, 1024),
+                    mma_bf16_ss(tmem + kColDQ + 64 * b, sdesc_sw128(sDS + 2048 * kk, 16384, 1024),
                                 sdesc_sw128(sK + 2048 * kk, 16384, 1024), kIdescDQ, kk > 0);
-                mma_commit(smem_u32(&bars.dq_full[s]));
-                mma_commit(smem_u32(&bars.ds_empty[s]));
+                mma_commit(smem_u32(&bars.dq_full[b]));
+                mma_commit(smem_u32(&bars.ds_empty[b]));
             }
             if (ok) mma_commit(smem_u32(&bars.all_done));
             if (!ok) record_timeout(args.ctl, &abort_flag);
@@ -242,81 +257,75 @@ __global__ void __launch_bounds__(kThreads, 1)
             const volatile int never = 0;
             mbar_wait(smem_u32(&bars.drain), 0, kDrainWaitNs, &never);
         }
-    } else if (warp >= 4 && warp < 8) {
-        // ================================================================ P / dS warpgroup
+    } else if (warp >= 4 && warp < 12) {
+        // ================================================================ P / dS warpgroups
+        const int half = (warp - 4) / 4;          // query columns 64*half .. 64*half+63
         const int wq = warp % 4;
         const int key_in_blk = wq * 32 + lane;
         const uint32_t lb = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-        const float c = args.c_log2;
+        const float2 c2 = make_float2(args.c_log2, args.c_log2);
         bool ok = true;
         for (int i = 0; i < n_q; ++i) {
-            const int s = i & 1;
-            ok = mbar_wait(smem_u32(&bars.q_full[s]), (i >> 1) & 1, lim, &abort_flag);
+            const int s = i % kQStages;
+            ok = mbar_wait(smem_u32(&bars.q_full[s]), (i / kQStages) & 1, lim, &abort_flag);
             if (ok) ok = mbar_wait(smem_u32(&bars.s_full), i & 1, lim, &abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            const float4* L4 = reinterpret_cast<const float4*>(sb_ptr + kOffL + s * kBlk * 4);
-            const float4* D4 = reinterpret_cast<const float4*>(sb_ptr + kOffDelta + s * kBlk * 4);
-            uint32_t pk[64];  // P^T row, bf16 pairs
+            // -lse_i * log2(e) and -delta_i of this block's 64 queries
+            const float2* L2 = reinterpret_cast<const float2*>(sb_ptr + kOffL + s * kBlk * 4) + 32 * half;
+            const float2* D2 = reinterpret_cast<const float2*>(sb_ptr + kOffDelta + s * kBlk * 4) + 32 * half;
+            uint32_t pk[32];  // P^T row (64 queries) as bf16 pairs
+            {
+                uint32_t r[2][32];
+                tmem_ld32(lb + kColS + 64 * half, r[0]);
+                tmem_ld32(lb + kColS + 64 * half + 32, r[1]);
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                uint32_t r[32];
-                tmem_ld32(lb + kColS + 32 * h, r);
-#pragma unroll
-                for (int g = 0; g < 8; ++g) {
-                    const float4 l4 = L4[8 * h + g];
-                    const float p0 = ex2_approx(fmaf(__uint_as_float(r[4 * g + 0]), c, -l4.x));
-                    const float p1 = ex2_approx(fmaf(__uint_as_float(r[4 * g + 1]), c, -l4.y));
-                    const float p2 = ex2_approx(fmaf(__uint_as_float(r[4 * g + 2]), c, -l4.z));
-                    const float p3 = ex2_approx(fmaf(__uint_as_float(r[4 * g + 3]), c, -l4.w));
-                    pk[16 * h + 2 * g] = pack_bf16x2(p0, p1);
-                    pk[16 * h + 2 * g + 1] = pack_bf16x2(p2, p3);
+                for (int x = 0; x < 32; ++x) {
+                    const uint32_t* rr = r[x / 16];
+                    const int e = 2 * (x % 16);
+                    const float2 a = __ffma2_rn(make_float2(__uint_as_float(rr[e]), __uint_as_float(rr[e + 1])),
+                                                c2, L2[x]);
+                    pk[x] = pack_bf16x2(ex2_approx(a.x), ex2_approx(a.y));
                 }
             }
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t w[32];
-#pragma unroll
-                for (int x = 0; x < 32; ++x) w[x] = pk[32 * h + x];
-                tmem_st32(lb + kColS + 32 * h, w);
-            }
+            // P^T of this half goes inside the columns this half read (the other half's
+            // scores may still be unread): queries 64h..64h+63 -> columns 64h..64h+31
+            tmem_st32(lb + kColS + 64 * half, pk);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(smem_u32(&bars.p_full));
 
             // dS^T = P^T o (dP^T - delta)
+            const int b = i & 1;
             ok = mbar_wait(smem_u32(&bars.dp_full), i & 1, lim, &abort_flag);
-            if (ok && i >= 2) ok = mbar_wait(smem_u32(&bars.ds_empty[s]), ((i >> 1) & 1) ^ 1, lim, &abort_flag);
+            if (ok && i >= 2) ok = mbar_wait(smem_u32(&bars.ds_empty[b]), ((i >> 1) & 1) ^ 1, lim, &abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            uint8_t* dsbuf = sb_ptr + kOffDS + s * kDSBytes;
+            uint8_t* dsrow = sb_ptr + kOffDS + b * kDSBytes + half * 16384 + key_in_blk * 128;
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
+            for (int h = 0; h < 2; ++h) {
                 uint32_t r[32];
-                tmem_ld32(lb + kColDP + 32 * h, r);
+                tmem_ld32(lb + kColDP + 64 * half + 32 * h, r);
                 uint32_t w[16];
 #pragma unroll
-                for (int g = 0; g < 8; ++g) {
-                    const float4 d4 = D4[8 * h + g];
-                    const uint32_t pa = pk[16 * h + 2 * g], pb = pk[16 * h + 2 * g + 1];
-                    const float p0 = __uint_as_float(pa << 16), p1 = __uint_as_float(pa & 0xFFFF0000u);
-                    const float p2 = __uint_as_float(pb << 16), p3 = __uint_as_float(pb & 0xFFFF0000u);
-                    w[2 * g] = pack_bf16x2(p0 * (__uint_as_float(r[4 * g + 0]) - d4.x),
-                                           p1 * (__uint_as_float(r[4 * g + 1]) - d4.y));
-                    w[2 * g + 1] = pack_bf16x2(p2 * (__uint_as_float(r[4 * g + 2]) - d4.z),
-                                               p3 * (__uint_as_float(r[4 * g + 3]) - d4.w));
+                for (int x = 0; x < 16; ++x) {
+                    const uint32_t pp = pk[16 * h + x];
+                    const float2 p = make_float2(__uint_as_float(pp << 16), __uint_as_float(pp & 0xFFFF0000u));
+                    const float2 g = __fadd2_rn(make_float2(__uint_as_float(r[2 * x]), __uint_as_float(r[2 * x + 1])),
+                                                D2[16 * h + x]);
+                    const float2 ds = __fmul2_rn(p, g);
+                    w[x] = pack_bf16x2(ds.x, ds.y);
                 }
-                tmem_st16(lb + kColDP + 16 * h, w);
-                // queries 32h..32h+31 of this key row -> MN-major swizzled A tile for dQ:
-                // column (query / 64), row = key, 16-byte granule (query % 64) / 8 ^ (key % 8)
-                const int col = h >> 1;
+                tmem_st16(lb + kColDP + 64 * half + 16 * h, w);
+                // queries 64*half + 32h .. +31 of this key row -> MN-major swizzled A tile
+                // for dQ: column `half`, row = key, 16-byte granule ((query % 64) / 8) ^ (key % 8)
 #pragma unroll
                 for (int g4 = 0; g4 < 4; ++g4) {
-                    const int gran = ((h & 1) * 4 + g4) ^ (key_in_blk & 7);
-                    uint4* dst = reinterpret_cast<uint4*>(dsbuf + col * 16384 + key_in_blk * 128 + gran * 16);
-                    *dst = make_uint4(w[4 * g4], w[4 * g4 + 1], w[4 * g4 + 2], w[4 * g4 + 3]);
+                    const int gran = (h * 4 + g4) ^ (key_in_blk & 7);
+                    *reinterpret_cast<uint4*>(dsrow + gran * 16) =
+                        make_uint4(w[4 * g4], w[4 * g4 + 1], w[4 * g4 + 2], w[4 * g4 + 3]);
                 }
             }
             tmem_st_wait();
@@ -324,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive(smem_u32(&bars.ds_full));
         }
-        // epilogue: dV rows of this key block
+        // epilogue: warps 4-7 store dV, warps 8-11 store dK (times scale)
         if (ok) {
             ok = mbar_wait(smem_u32(&bars.all_done), 0, lim, &abort_flag);
             ok = __all_sync(0xffffffffu, ok);
@@ -334,65 +343,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
             tc_fence_after();
             const int key = kvb * kBlk + key_in_blk;
-            uint16_t* out = static_cast<uint16_t*>(args.dv) + (static_cast<size_t>(bh) * N + key) * kD;
+            const float sc = half ? args.scale : 1.0f;
+            void* dst = half ? args.dk : args.dv;
+            const uint32_t col = half ? kColDK : kColDV;
+            uint16_t* out = static_cast<uint16_t*>(dst) + (static_cast<size_t>(bh) * N + key) * kD;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 uint32_t r[32];
-                tmem_ld32(lb + kColDV + 32 * h, r);
-                if (key < N) {
-                    uint4* o4 = reinterpret_cast<uint4*>(out + 32 * h);
-#pragma unroll
-                    for (int x = 0; x < 4; ++x)
-                        o4[x] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * x]), __uint_as_float(r[8 * x + 1])),
-                                           pack_bf16x2(__uint_as_float(r[8 * x + 2]), __uint_as_float(r[8 * x + 3])),
-                                           pack_bf16x2(__uint_as_float(r[8 * x + 4]), __uint_as_float(r[8 * x + 5])),
-                                           pack_bf16x2(__uint_as_float(r[8 * x + 6]), __uint_as_float(r[8 * x + 7])));
-                }
-            }
-        }
-    } else if (warp >= 8) {
-        // ================================================================ dQ warpgroup
-        const int wq = warp % 4;
-        const int row_in_blk = wq * 32 + lane;
-        const uint32_t lb = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-        bool ok = true;
-        for (int i = 0; i < n_q; ++i) {
-            const int s = i & 1;
-            ok = mbar_wait(smem_u32(&bars.dq_full[s]), (i >> 1) & 1, lim, &abort_flag);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            tc_fence_after();
-            uint32_t r[2][32];
-            tmem_ld32(lb + kColDQ + 64 * s, r[0]);
-            tmem_ld32(lb + kColDQ + 64 * s + 32, r[1]);
-            tc_fence_before();
-            mbar_arrive(smem_u32(&bars.dq_free[s]));
-            float* acc = args.dq_acc + (static_cast<size_t>(bh) * Np + static_cast<size_t>(i) * kBlk + row_in_blk) * kD;
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-                for (int x = 0; x < 8; ++x)
-                    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(acc + 32 * h + 4 * x),
-                                 "f"(__uint_as_float(r[h][4 * x])), "f"(__uint_as_float(r[h][4 * x + 1])),
-                                 "f"(__uint_as_float(r[h][4 * x + 2])), "f"(__uint_as_float(r[h][4 * x + 3]))
-                                 : "memory");
-        }
-        // epilogue: dK rows of this key block, times scale
-        if (ok) {
-            ok = mbar_wait(smem_u32(&bars.all_done), 0, lim, &abort_flag);
-            ok = __all_sync(0xffffffffu, ok);
-        }
-        if (!ok) {
-            if (lane == 0) record_timeout(args.ctl, &abort_flag);
-        } else {
-            tc_fence_after();
-            const int key = kvb * kBlk + row_in_blk;
-            const float sc = args.scale;
-            uint16_t* out = static_cast<uint16_t*>(args.dk) + (static_cast<size_t>(bh) * N + key) * kD;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t r[32];
-                tmem_ld32(lb + kColDK + 32 * h, r);
+                tmem_ld32(lb + col + 32 * h, r);
                 if (key < N) {
                     uint4* o4 = reinterpret_cast<uint4*>(out + 32 * h);
 #pragma unroll
@@ -405,6 +363,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+    } else if (warp >= 12) {
+        // ================================================================ dQ drain
+        const int wq = warp % 4;
+        const int row_in_blk = wq * 32 + lane;
+        const uint32_t lb = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+        bool ok = true;
+        for (int i = 0; i < n_q; ++i) {
+            const int b = i & 1;
+            ok = mbar_wait(smem_u32(&bars.dq_full[b]), (i >> 1) & 1, lim, &abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t r[2][32];
+            tmem_ld32(lb + kColDQ + 64 * b, r[0]);
+            tmem_ld32(lb + kColDQ + 64 * b + 32, r[1]);
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bars.dq_free[b]));
+            float* acc = args.dq_acc + (static_cast<size_t>(bh) * Np + static_cast<size_t>(i) * kBlk + row_in_blk) * kD;
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int x = 0; x < 8; ++x)
+                    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(acc + 32 * h + 4 * x),
+                                 "f"(__uint_as_float(r[h][4 * x])), "f"(__uint_as_float(r[h][4 * x + 1])),
+                                 "f"(__uint_as_float(r[h][4 * x + 2])), "f"(__uint_as_float(r[h][4 * x + 3]))
+                                 : "memory");
+        }
+        if (!ok && lane == 0) record_timeout(args.ctl, &abort_flag);
     }
 
     tc_fence_before();
@@ -416,8 +402,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------- pre / post passes
-// delta_i = dO_i . O_i, lse2_i = lse_i * log2(e) (rows past N: delta 0, lse2 +inf
-// so that recomputed P is exactly 0 there), dQ accumulator zeroed.
+// -delta_i = -(dO_i . O_i) and -lse_i * log2(e) (rows past N: 0 and -inf, so
+// that recomputed P is exactly 0 there), dQ accumulator zeroed.  Both are stored
+// negated so the main kernel adds them with packed FMA/FADD.
 // 8 threads per row, each reading 16 bytes of O and dO.
 __global__ void bwd_prep_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dO,
                                 const float* __restrict__ lse, float* __restrict__ ws_delta,
@@ -445,8 +432,8 @@ __global__ void bwd_prep_kernel(const uint4* __restrict__ o, const uint4* __rest
         sum += __shfl_xor_sync(0xffffffffu, sum, 2);
         sum += __shfl_xor_sync(0xffffffffu, sum, 4);
         if (part == 0) {
-            ws_delta[r] = sum;
-            ws_lse2[r] = (i < N) ? lse[static_cast<size_t>(bh) * N + i] * kLog2e : INFINITY;
+            ws_delta[r] = -sum;
+            ws_lse2[r] = (i < N) ? -lse[static_cast<size_t>(bh) * N + i] * kLog2e : -INFINITY;
         }
     }
     const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
