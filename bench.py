@@ -152,7 +152,7 @@ def make_part(torch, fa, inputs, part, dev):
     return P
 
 
-def run_part(fa, P, stream):
+def run_part(fa, P, stream, mid_event=None):
     name, kind, dt, B, H, N, d, causal = P["part"]
     D = P["dev"]
     if kind == "fwd8":
@@ -162,6 +162,8 @@ def run_part(fa, P, stream):
     else:
         fa.fa_fwd(D["q"], D["k"], D["v"], P["o"], P["lse"], P["scale"], causal, fa.FA_BF16, stream)
     if kind == "fwdbwd":
+        if mid_event is not None:
+            mid_event.record(stream)
         fa.fa_bwd(D["q"], D["k"], D["v"], P["o"], P["lse"], D["do"], P["dq"], P["dk"], P["dv"],
                   P["ws"], P["scale"], False, fa.FA_BF16, stream)
 
@@ -265,10 +267,10 @@ def bench_ours(args):
             dist.barrier()
         torch.cuda.synchronize()
 
-    def step_timed(events):
+    def step_timed(events, mids):
         for i, P in enumerate(parts):
             events[i].record(stream)
-            run_part(fa, P, stream)
+            run_part(fa, P, stream, mids[i])
         events[-1].record(stream)
 
     for _ in range(args.warmup):
@@ -280,13 +282,16 @@ def bench_ours(args):
 
     K = args.steps
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(parts) + 1)] for _ in range(K)]
+    # an extra event between the forward and the backward of the fwd+bwd part
+    mids = [[torch.cuda.Event(enable_timing=True) if P["part"][1] == "fwdbwd" else None
+             for P in parts] for _ in range(K)]
     barrier()
     with ClockSampler(local) as clk:
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
         for k in range(K):
-            step_timed(evs[k])
+            step_timed(evs[k], mids[k])
         t_end.record(stream)
         barrier()
     total_ms = t_start.elapsed_time(t_end)
@@ -294,6 +299,9 @@ def bench_ours(args):
     if st != 0:
         raise RuntimeError(f"device status {fa.fa_status_string(st)}")
     part_ms = [[evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(K)] for i in range(len(parts))]
+    split_ms = {i: ([evs[k][i].elapsed_time(mids[k][i]) for k in range(K)],
+                    [mids[k][i].elapsed_time(evs[k][i + 1]) for k in range(K)])
+                for i, P in enumerate(parts) if P["part"][1] == "fwdbwd"}
 
     # e2e: same step with pinned host buffers, copies inside the timed region
     Ke = max(3, K // 10)
@@ -328,6 +336,15 @@ def bench_ours(args):
         part_out[name] = {"ms": round(mean, 4), "best_ms": round(min(ms), 4),
                           "tflops": round(tf, 1), "pct_of_peak": round(100 * tf / peak, 1),
                           "peak_tflops": round(peak, 1), "flop": P["flop"]}
+
+    for i, (fms, bms) in split_ms.items():
+        name, kind, dt, B, H, N, d, causal = parts[i]["part"]
+        for sub, ms, f in (("fwd", fms, flops("fwd", B, H, N, d, causal)),
+                           ("bwd", bms, flops("fwdbwd", B, H, N, d, causal) - flops("fwd", B, H, N, d, causal))):
+            mean = sum(ms) / len(ms)
+            tf = f / (mean * 1e-3) / 1e12
+            part_out[name][sub] = {"ms": round(mean, 4), "tflops": round(tf, 1),
+                                   "pct_of_peak": round(100 * tf / pk["bf16"], 1)}
 
     dom = part_out[PARTS[0][0]]
     roofline = {"kernel": "fwd_sm103_kernel<128,bf16> (B1 H32 N16384 d128 non-causal)",
