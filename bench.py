@@ -54,6 +54,21 @@ def flops(kind, B, H, N, d, causal):
     return f / 2 if causal else f
 
 
+def dominant_traffic():
+    """DRAM bytes per launch of the dominant kernel from the committed ncu capture
+    (profiles/roofline_traffic.json), or None if its sources changed since."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "roofline_traffic.json")
+    if not os.path.exists(path):
+        return None
+    rec = json.load(open(path))
+    h = hashlib.sha256()
+    for f in rec["source_files"]:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return rec["traffic_bytes_per_launch"] if h.hexdigest() == rec["source_sha256"] else None
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -351,7 +366,9 @@ def bench_ours(args):
                 "bound": "tensor", "achieved": dom["tflops"], "peak": pk["bf16"],
                 "unit": "TFLOP/s", "frac": round(dom["tflops"] / pk["bf16"], 4),
                 "peak_source": f"{pk['source']} bf16 burst (sustained {pk['bf16_sustained']})",
-                "traffic": args.traffic}
+                "traffic": dominant_traffic(),
+                "traffic_unit": "bytes per launch (ncu dram read+write)",
+                "algorithmic_bytes": 4 * 1 * 32 * 16384 * 128 * 2 + 32 * 16384 * 4}
 
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
@@ -420,8 +437,6 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
-    ap.add_argument("--traffic", type=float, default=None,
-                    help="DRAM bytes per launch of the dominant kernel from an ncu capture")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
