@@ -69,6 +69,23 @@ def dominant_traffic():
     return rec["traffic_bytes_per_launch"] if h.hexdigest() == rec["source_sha256"] else None
 
 
+def max_over_ranks(values, device=None):
+    """Element-wise max of per-rank timings over the process group (the slowest rank
+    sets the job's time); the values unchanged when not distributed."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def job_tflops(world, step_flop, ms_step):
+    """Whole-job throughput: each of `world` replicas runs one step in ms_step."""
+    return world * step_flop / (ms_step * 1e-3) / 1e12
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -333,12 +350,9 @@ def bench_ours(args):
     e2e_ms = e0.elapsed_time(e1) / Ke
 
     ms_step = total_ms / K
-    if world > 1:
-        t = torch.tensor([ms_step, e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step, e2e_ms = float(t[0]), float(t[1])
+    ms_step, e2e_ms = max_over_ranks([ms_step, e2e_ms], dev)
     step_flop = sum(P["flop"] for P in parts)
-    value = world * step_flop / (ms_step * 1e-3) / 1e12
+    value = job_tflops(world, step_flop, ms_step)
     pk = peaks()
     fp8_tf, fp8_how = fp8_peak(torch, dev)
 
@@ -380,7 +394,7 @@ def bench_ours(args):
         "parts": part_out,
         "fp8_peak_tflops": None if fp8_tf is None else round(fp8_tf, 1), "fp8_peak_how": fp8_how,
         "roofline": roofline,
-        "e2e": {"value": round(world * step_flop / (e2e_ms * 1e-3) / 1e12, 1), "unit": UNIT,
+        "e2e": {"value": round(job_tflops(world, step_flop, e2e_ms), 1), "unit": UNIT,
                 "ms_per_step": round(e2e_ms, 3),
                 "h2d_bytes_per_step": sum(P["h2d"] for P in parts),
                 "d2h_bytes_per_step": sum(P["d2h"] for P in parts)},
