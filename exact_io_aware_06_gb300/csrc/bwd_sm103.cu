@@ -73,7 +73,8 @@ struct BwdArgs {
     float* dq_acc;          // [BH][Np][d]
     void* dk;
     void* dv;
-    int N, Np, n_kv;
+    int N, Np, n_kv, BH;
+    int causal;             // 1: key j only reaches queries i >= j
     float c_log2;           // scale * log2(e)
     float scale;
     DevCtl ctl;
@@ -106,10 +107,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sb = (smem_u32(smem_raw) + 1023u) & ~1023u;
     uint8_t* const sb_ptr = smem_raw + (sb - smem_u32(smem_raw));
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int bh = blockIdx.x / args.n_kv;
-    const int kvb = blockIdx.x % args.n_kv;
+    // causal: the key block with the most query blocks (kvb = 0) goes first for every head
+    const int bh = args.causal ? static_cast<int>(blockIdx.x % args.BH) : static_cast<int>(blockIdx.x / args.n_kv);
+    const int kvb = args.causal ? static_cast<int>(blockIdx.x / args.BH) : static_cast<int>(blockIdx.x % args.n_kv);
     const int N = args.N, Np = args.Np;
     const int n_q = Np / kBlk;
+    // query blocks this key block meets: all of them, or (causal) blocks kvb..n_q-1.
+    // Loops run over the local index i (barrier phases, stages, buffers); the query
+    // block itself is i0 + i.
+    const int i0 = args.causal ? kvb : 0;
+    const int n_loc = n_q - i0;
     const uint64_t lim = args.ctl.wait_ns;
 
     if (threadIdx.x == 0) {
@@ -156,8 +163,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(sb + kOffV, &tm_v, kvf, 0, kvb * kBlk, bh);
             int issued = 0;
             bool ok = true;
-            for (int i = 0; i < n_q; ++i) {
+            for (int i = 0; i < n_loc; ++i) {
                 const int s = i % kQStages;
+                const int qb = i0 + i;
                 if (i >= kQStages &&
                     !mbar_wait(smem_u32(&bars.q_empty[s]), ((i / kQStages) & 1) ^ 1, lim, &abort_flag)) {
                     ok = false;
@@ -165,9 +173,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const uint32_t qf = smem_u32(&bars.q_full[s]);
                 mbar_arrive_expect_tx(qf, 2 * kTile + 2 * kBlk * 4);
-                tma_load_3d(sb + kOffQ + s * kTile, &tm_q, qf, 0, i * kBlk, bh);
-                tma_load_3d(sb + kOffDO + s * kTile, &tm_do, qf, 0, i * kBlk, bh);
-                const size_t row = static_cast<size_t>(bh) * Np + static_cast<size_t>(i) * kBlk;
+                tma_load_3d(sb + kOffQ + s * kTile, &tm_q, qf, 0, qb * kBlk, bh);
+                tma_load_3d(sb + kOffDO + s * kTile, &tm_do, qf, 0, qb * kBlk, bh);
+                const size_t row = static_cast<size_t>(bh) * Np + static_cast<size_t>(qb) * kBlk;
                 bulk_load(sb + kOffL + s * kBlk * 4, args.ws_lse2 + row, kBlk * 4, qf);
                 bulk_load(sb + kOffDelta + s * kBlk * 4, args.ws_delta + row, kBlk * 4, qf);
                 issued = i + 1;
@@ -206,10 +214,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 issue_s(0);
                 issue_dp(0);
             }
-            for (int i = 0; i < n_q && ok; ++i) {
+            for (int i = 0; i < n_loc && ok; ++i) {
                 const int s = i % kQStages;
                 const int s1 = (i + 1) % kQStages;
-                const bool more = i + 1 < n_q;
+                const bool more = i + 1 < n_loc;
                 const uint32_t sQ = sb + kOffQ + s * kTile, sDO = sb + kOffDO + s * kTile;
                 // dV += P^T dO_i
                 ok = mbar_wait(smem_u32(&bars.p_full), i & 1, lim, &abort_flag);
@@ -265,8 +273,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lb = tmem + (static_cast<uint32_t>(wq * 32) << 16);
         const float2 c2 = make_float2(args.c_log2, args.c_log2);
         bool ok = true;
-        for (int i = 0; i < n_q; ++i) {
+        for (int i = 0; i < n_loc; ++i) {
             const int s = i % kQStages;
+            // causal diagonal block: key k only reaches queries q >= k of the block
+            const bool diag = args.causal && (i0 + i == kvb);
             ok = mbar_wait(smem_u32(&bars.q_full[s]), (i / kQStages) & 1, lim, &abort_flag);
             if (ok) ok = mbar_wait(smem_u32(&bars.s_full), i & 1, lim, &abort_flag);
             ok = __all_sync(0xffffffffu, ok);
@@ -284,8 +294,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int x = 0; x < 32; ++x) {
                     const uint32_t* rr = r[x / 16];
                     const int e = 2 * (x % 16);
-                    const float2 a = __ffma2_rn(make_float2(__uint_as_float(rr[e]), __uint_as_float(rr[e + 1])),
-                                                c2, L2[x]);
+                    float2 a = __ffma2_rn(make_float2(__uint_as_float(rr[e]), __uint_as_float(rr[e + 1])),
+                                          c2, L2[x]);
+                    if (diag) {
+                        const int q0 = 64 * half + 32 * (x / 16) + e;
+                        if (key_in_blk > q0) a.x = -INFINITY;
+                        if (key_in_blk > q0 + 1) a.y = -INFINITY;
+                    }
                     pk[x] = pack_bf16x2(ex2_approx(a.x), ex2_approx(a.y));
                 }
             }
@@ -369,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row_in_blk = wq * 32 + lane;
         const uint32_t lb = tmem + (static_cast<uint32_t>(wq * 32) << 16);
         bool ok = true;
-        for (int i = 0; i < n_q; ++i) {
+        for (int i = 0; i < n_loc; ++i) {
             const int b = i & 1;
             ok = mbar_wait(smem_u32(&bars.dq_full[b]), (i >> 1) & 1, lim, &abort_flag);
             ok = __all_sync(0xffffffffu, ok);
@@ -380,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld32(lb + kColDQ + 64 * b + 32, r[1]);
             tc_fence_before();
             mbar_arrive(smem_u32(&bars.dq_free[b]));
-            float* acc = args.dq_acc + (static_cast<size_t>(bh) * Np + static_cast<size_t>(i) * kBlk + row_in_blk) * kD;
+            float* acc = args.dq_acc + (static_cast<size_t>(bh) * Np + static_cast<size_t>(i0 + i) * kBlk + row_in_blk) * kD;
 #pragma unroll
             for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -472,7 +487,7 @@ size_t bwd_workspace_bytes(int BH, int N, int d) {
 
 int launch_bwd_sm103(const void* q, const void* k, const void* v, const void* o, const float* lse,
                      const void* dO, void* dq, void* dk, void* dv, void* workspace, int BH, int N,
-                     int d, float scale, DevCtl ctl, cudaStream_t s) {
+                     int d, float scale, int causal, DevCtl ctl, cudaStream_t s) {
     if (d != kD) return -1;
     const int Np = round_up(N, kBlk);
     float* ws = static_cast<float*>(workspace);
@@ -517,6 +532,8 @@ int launch_bwd_sm103(const void* q, const void* k, const void* v, const void* o,
     a.N = N;
     a.Np = Np;
     a.n_kv = Np / kBlk;
+    a.BH = BH;
+    a.causal = causal ? 1 : 0;
     a.c_log2 = scale * kLog2e;
     a.scale = scale;
     a.ctl = ctl;

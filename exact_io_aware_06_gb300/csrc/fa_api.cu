@@ -160,14 +160,14 @@ __attribute__((visibility("default"))) int fa_bwd(const void* q, const void* k, 
         return FA_ERR_INVALID_ARG;
     if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
     if (dtype != FA_F32 && dtype != FA_BF16 && dtype != FA_E4M3) return FA_ERR_INVALID_ARG;
-    if (dtype != FA_BF16 || d != 64 || causal) return FA_ERR_UNSUPPORTED;
+    if (dtype != FA_BF16 || d != 64) return FA_ERR_UNSUPPORTED;
     if (workspace_bytes < bwd_workspace_bytes(B * H, N, d)) return FA_ERR_INVALID_ARG;
     int err = FA_OK;
     int* st = status_word(&err);
     if (st == nullptr) return err;
     DevCtl ctl{st, g_wait_ns.load()};
     return from_cuda(launch_bwd_sm103(q, k, v, o, lse, dO, dq, dk, dv, workspace, B * H, N, d,
-                                      scale, ctl, static_cast<cudaStream_t>(stream)));
+                                      scale, causal ? 1 : 0, ctl, static_cast<cudaStream_t>(stream)));
 }
 
 __attribute__((visibility("default"))) int fa_last_device_error(void* stream) {

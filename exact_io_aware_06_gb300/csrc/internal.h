@@ -32,13 +32,13 @@ int launch_fwd_sm103(const void* q, const void* k, const void* v, void* o, float
                      DevCtl ctl, cudaStream_t s);
 
 // Backward pieces.  Workspace layout (all float32, Np = N rounded up to 128):
-//   [0, BH*Np)            delta_i = dO_i . O_i
-//   [BH*Np, 2*BH*Np)      lse_i * log2(e)
+//   [0, BH*Np)            -delta_i = -(dO_i . O_i)
+//   [BH*Np, 2*BH*Np)      -lse_i * log2(e)   (both negated for packed FMA/FADD use)
 //   [2*BH*Np, ...)        dQ accumulator [BH][Np][d]
 size_t bwd_workspace_bytes(int BH, int N, int d);
 int launch_bwd_sm103(const void* q, const void* k, const void* v, const void* o, const float* lse,
                      const void* dO, void* dq, void* dk, void* dv, void* workspace, int BH, int N,
-                     int d, float scale, DevCtl ctl, cudaStream_t s);
+                     int d, float scale, int causal, DevCtl ctl, cudaStream_t s);
 
 // A kernel that waits on a barrier nobody arrives at, with the bounded wait;
 // it must record kDevTimeout and return.

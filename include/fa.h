@@ -114,9 +114,11 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d);
  *                    owned by the caller; its contents on entry do not matter
  *                    and on return are unspecified.  Calls that overlap in time
  *                    must not share one workspace.
- *   dtype          : FA_BF16.   d : 64.   causal : 0.
+ *   dtype          : FA_BF16.   d : 64.
+ *   causal         : 0, or 1 for the causal mask of the forward (key j reaches
+ *                    only queries i >= j; lse must come from a causal forward).
  * Errors: FA_ERR_INVALID_ARG (null/misaligned pointers, workspace too small,
- * bad sizes), FA_ERR_UNSUPPORTED (other dtype or d, causal = 1),
+ * bad sizes), FA_ERR_UNSUPPORTED (other dtype or d),
  * FA_ERR_CUDA (launch failure).
  */
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,

@@ -108,4 +108,3 @@ def test_bwd_argument_errors(L):
     assert b(dtype=9) == 1
     assert b(dtype=0) == 2
     assert b(d=128) == 2
-    assert b(causal=1) == 2

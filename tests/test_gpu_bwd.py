@@ -17,20 +17,21 @@ def _built():
     ensure_built()
 
 
-def run_bwd(dev, scale):
+def run_bwd(dev, scale, causal=False):
     q, k, v, do = dev["q"], dev["k"], dev["v"], dev["do"]
-    o, lse = fa.attention_forward(q, k, v, scale)
-    dq, dk, dv = fa.attention_backward(q, k, v, o, lse, do, scale)
+    o, lse = fa.attention_forward(q, k, v, scale, causal)
+    dq, dk, dv = fa.attention_backward(q, k, v, o, lse, do, scale, causal)
     check_status()
     return dq, dk, dv
 
 
 @pytest.mark.parametrize("N", [1, 17, 128, 130, 255, 384, 700])
-def test_bwd_small(N):
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_small(N, causal):
     x, dev = device_inputs(1, 2, N, 64, "bf16", with_do=True)
     s = scale_for(64)
-    got = run_bwd(dev, s)
-    ref = oracle.attn_bwd(f64(x["q"]), f64(x["k"]), f64(x["v"]), f64(x["do"]), s)
+    got = run_bwd(dev, s, causal)
+    ref = oracle.attn_bwd(f64(x["q"]), f64(x["k"]), f64(x["v"]), f64(x["do"]), s, causal)
     for name, g, r in zip(("dq", "dk", "dv"), got, ref):
         assert max_err(f64(g), r) <= TOL_BF16_GRAD, name
 
@@ -62,3 +63,19 @@ def test_bwd_workspace_reuse_and_determinism_of_dk_dv():
     # dQ goes through float atomics, so only close
     assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
     assert max_err(f64(a[0]), f64(b[0])) <= 1e-2
+
+
+def test_bwd_causal_b4_h16_n2048_d64_sampled_heads():
+    # causal backward at the backward workload's size; whole heads against the oracle
+    B, H, N, d = 4, 16, 2048, 64
+    x, dev = device_inputs(B, H, N, d, "bf16", with_do=True)
+    s = scale_for(d)
+    dq, dk, dv = (f64(t) for t in run_bwd(dev, s, causal=True))
+    for b, h in ((0, 3), (2, 15)):
+        ref = oracle.attn_bwd(f64(x["q"][b, h]), f64(x["k"][b, h]), f64(x["v"][b, h]),
+                              f64(x["do"][b, h]), s, causal=True)
+        for name, g, r in zip(("dq", "dk", "dv"), (dq[b, h], dk[b, h], dv[b, h]), ref):
+            assert max_err(g, r) <= TOL_BF16_GRAD, name
+    # query 0 sees only key 0: O_0 = V_0, so dS_00 = dO_0 . (V_0 - O_0) = 0 and dQ_0 = 0
+    assert np.isfinite(dv).all() and np.isfinite(dq).all()
+    assert np.abs(dq[:, :, 0]).max() <= 1e-2
