@@ -14,7 +14,8 @@ import math
 import os
 
 __all__ = [
-    "FaError", "FA_F32", "FA_BF16", "FA_E4M3", "lib", "fa_fwd", "fa_fwd_fp8", "fa_bwd",
+    "FaError", "FA_F32", "FA_BF16", "FA_E4M3", "lib", "fa_fwd", "fa_fwd_fp8", "fa_fwd_gqa",
+    "fa_fwd_fp8_per_head", "fa_bwd",
     "fa_bwd_workspace_size", "fa_bwd_noalloc", "fa_last_device_error", "fa_set_wait_timeout_ns",
     "fa_selftest_wait_timeout", "fa_status_string", "attention_forward", "attention_backward",
 ]
@@ -47,6 +48,10 @@ def lib():
         L.fa_fwd.restype = i
         L.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, f, f, f, i, i, i, i, f, i, vp]
         L.fa_fwd_fp8.restype = i
+        L.fa_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
+        L.fa_fwd_gqa.restype = i
+        L.fa_fwd_fp8_per_head.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+        L.fa_fwd_fp8_per_head.restype = i
         L.fa_bwd_workspace_size.argtypes = [i, i, i, i]
         L.fa_bwd_workspace_size.restype = sz
         L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, f, i, i, vp]
@@ -109,6 +114,28 @@ def fa_fwd_fp8(q8, k8, v8, o, lse, q_descale, k_descale, v_descale, scale, causa
     _check(lib().fa_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(o), _ptr(lse), float(q_descale),
                             float(k_descale), float(v_descale), B, H, N, d, float(scale),
                             int(bool(causal)), _stream(stream)), "fa_fwd_fp8")
+
+
+def fa_fwd_gqa(q, k, v, o, lse, scale, causal, dtype, stream=None):
+    """Grouped-query forward: q, o [B, H, N, d]; k, v [B, H_kv, N, d] with H % H_kv == 0."""
+    B, H, N, d = _shape(q)
+    H_kv = _shape(k)[1]
+    _check(lib().fa_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, H_kv, N, d,
+                            float(scale), int(bool(causal)), int(dtype), _stream(stream)),
+           "fa_fwd_gqa")
+
+
+def fa_fwd_fp8_per_head(q8, k8, v8, o, lse, q_descale, k_descale, v_descale, scale, causal,
+                        stream=None):
+    """FP8 forward with per-(b, h) descales: float32 device tensors of B*H elements."""
+    B, H, N, d = _shape(q8)
+    for t in (q_descale, k_descale, v_descale):
+        if t.numel() != B * H or t.dtype.itemsize != 4 or not t.is_contiguous():
+            raise ValueError("per-head descales: contiguous float32, B*H elements")
+    _check(lib().fa_fwd_fp8_per_head(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(o), _ptr(lse),
+                                     _ptr(q_descale), _ptr(k_descale), _ptr(v_descale), B, H, N,
+                                     d, float(scale), int(bool(causal)), _stream(stream)),
+           "fa_fwd_fp8_per_head")
 
 
 def fa_bwd_workspace_size(B, H, N, d):

@@ -53,6 +53,10 @@ struct FwdArgs {
     float c_log2;     // scale * log2(e) (times the FP8 descales)
     float o_scale;    // multiplies O at the end (FP8: v descale), 1 otherwise
     int causal;
+    int H, H_kv;                 // query heads and K/V heads per batch (H % H_kv == 0)
+    const float* qk_descale_q;   // optional per-(b, h) FP8 descales (device); null: none
+    const float* qk_descale_k;   //   indexed by the tensor's own head (b*H + h / b*H_kv + g)
+    const float* v_descale;
     DevCtl ctl;
 };
 
@@ -175,6 +179,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- tile coordinates: within a head, heaviest (last) query pair first
     const int bh = blockIdx.x / args.n_pairs;
+    // grouped-query attention: H / H_kv query heads share one K/V head
+    const int bh_kv = (bh / args.H) * args.H_kv + (bh % args.H) / (args.H / args.H_kv);
     const int pair = args.n_pairs - 1 - (blockIdx.x % args.n_pairs);
     const int r0 = pair * 2 * kBM;
     const int N = args.N;
@@ -239,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive_expect_tx(kf, C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c)
                     tma_load_3d(smem_base + C::kOffK + s * C::kTileBytes + c * C::kChunkBytes, &tm_k,
-                                kf, c * C::kBoxX, j * kBN, bh);
+                                kf, c * C::kBoxX, j * kBN, bh_kv);
                 if (j >= kStages && !mbar_wait(smem_u32(&bars.v_empty[s]), ph, lim, &abort_flag)) {
                     issued = 2 * j + 1;
                     ok = false;
@@ -249,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive_expect_tx(vf, C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c)
                     tma_load_3d(smem_base + C::kOffV + s * C::kTileBytes + c * C::kChunkBytes, &tm_v,
-                                vf, c * C::kBoxX, j * kBN, bh);
+                                vf, c * C::kBoxX, j * kBN, bh_kv);
                 issued = 2 * j + 2;
             }
             if (!ok) record_timeout(args.ctl, &abort_flag);
@@ -353,7 +359,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
         const uint32_t colS = t ? C::kColS1 : C::kColS0;
         const uint32_t colO = t ? C::kColO1 : C::kColO0;
-        const float c = args.c_log2;
+        // per-head FP8 descales fold into the score constant and the output scale
+        const float c = args.qk_descale_q
+                            ? args.c_log2 * args.qk_descale_q[bh] * args.qk_descale_k[bh_kv]
+                            : args.c_log2;
+        const float o_scale = args.v_descale ? args.v_descale[bh_kv] : args.o_scale;
         const bool c_pos = c >= 0.f;
         // a masked score must become -inf after the multiply by c
         const uint32_t mask_bits = c_pos ? 0xff800000u : 0x7f800000u;
@@ -454,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) record_timeout(args.ctl, &abort_flag);
         } else {
             tc_fence_after();
-            const float inv = args.o_scale / l;
+            const float inv = o_scale / l;
             const size_t orow = (static_cast<size_t>(bh) * N + qrow) * D;
 #pragma unroll
             for (int q4 = 0; q4 < D / 32; ++q4) {
@@ -486,15 +496,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int D, bool FP8>
-int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse, int BH, int N,
-                float c_log2, float o_scale, int causal, DevCtl ctl, cudaStream_t s) {
+int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                int H_kv, int N, float c_log2, float o_scale, const float* qd, const float* kd,
+                const float* vd, int causal, DevCtl ctl, cudaStream_t s) {
+    const int BH = B * H, BH_kv = B * H_kv;
     using C = Cfg<D, FP8>;
     const CUtensorMapDataType dt =
         FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     CUtensorMap tq, tk, tv;
     int rc = make_map_3d(&tq, q, dt, C::kElem, D, N, BH, C::kBoxX, kBM);
-    if (rc == 0) rc = make_map_3d(&tk, k, dt, C::kElem, D, N, BH, C::kBoxX, kBN);
-    if (rc == 0) rc = make_map_3d(&tv, v, dt, C::kElem, D, N, BH, C::kBoxX, kBN);
+    if (rc == 0) rc = make_map_3d(&tk, k, dt, C::kElem, D, N, BH_kv, C::kBoxX, kBN);
+    if (rc == 0) rc = make_map_3d(&tv, v, dt, C::kElem, D, N, BH_kv, C::kBoxX, kBN);
     if (rc != 0) return rc;
     static uint64_t attr_set = 0;  // per template instance, one bit per device
     int dev = 0;
@@ -514,6 +526,11 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse
     a.c_log2 = c_log2;
     a.o_scale = o_scale;
     a.causal = causal;
+    a.H = H;
+    a.H_kv = H_kv;
+    a.qk_descale_q = qd;
+    a.qk_descale_k = kd;
+    a.v_descale = vd;
     a.ctl = ctl;
     dim3 grid(a.n_pairs * BH);
     fwd_sm103_kernel<D, FP8><<<grid, kThreads, C::kSmemAlloc, s>>>(tq, tk, tv, a);
@@ -522,12 +539,18 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse
 
 }  // namespace
 
-int launch_fwd_sm103(const void* q, const void* k, const void* v, void* o, float* lse, int BH,
-                     int N, int d, float c_log2, float o_scale, int causal, bool is_fp8,
-                     DevCtl ctl, cudaStream_t s) {
-    if (is_fp8) return launch_impl<128, true>(q, k, v, o, lse, BH, N, c_log2, o_scale, causal, ctl, s);
-    if (d == 64) return launch_impl<64, false>(q, k, v, o, lse, BH, N, c_log2, o_scale, causal, ctl, s);
-    return launch_impl<128, false>(q, k, v, o, lse, BH, N, c_log2, o_scale, causal, ctl, s);
+int launch_fwd_sm103(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int H, int H_kv, int N, int d, float c_log2, float o_scale, const float* qd,
+                     const float* kd, const float* vd, int causal, bool is_fp8, DevCtl ctl,
+                     cudaStream_t s) {
+    if (is_fp8)
+        return launch_impl<128, true>(q, k, v, o, lse, B, H, H_kv, N, c_log2, o_scale, qd, kd, vd,
+                                      causal, ctl, s);
+    if (d == 64)
+        return launch_impl<64, false>(q, k, v, o, lse, B, H, H_kv, N, c_log2, o_scale, qd, kd, vd,
+                                      causal, ctl, s);
+    return launch_impl<128, false>(q, k, v, o, lse, B, H, H_kv, N, c_log2, o_scale, qd, kd, vd,
+                                   causal, ctl, s);
 }
 
 }  // namespace fa

@@ -26,10 +26,13 @@ cudaError_t launch_fwd_f32(const float* q, const float* k, const float* v, float
                            int BH, int N, int d, float scale, int causal, cudaStream_t s);
 
 // tcgen05 forward: bf16 (is_fp8 = false) or E4M3 inputs (is_fp8 = true, d = 128).
+// K/V have B*H_kv heads (H_kv = H: plain attention; H_kv < H: grouped-query).
+// qd/kd/vd: optional per-head FP8 descales on the device (null: use c_log2/o_scale only).
 // Returns 0 on success, or a CUDA / tensor-map error code (non-zero).
-int launch_fwd_sm103(const void* q, const void* k, const void* v, void* o, float* lse, int BH,
-                     int N, int d, float score_scale_log2, float o_scale, int causal, bool is_fp8,
-                     DevCtl ctl, cudaStream_t s);
+int launch_fwd_sm103(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int H, int H_kv, int N, int d, float c_log2, float o_scale, const float* qd,
+                     const float* kd, const float* vd, int causal, bool is_fp8, DevCtl ctl,
+                     cudaStream_t s);
 
 // Backward pieces.  Workspace layout (all float32, Np = N rounded up to 128):
 //   [0, BH*Np)            -delta_i = -(dO_i . O_i)

@@ -46,6 +46,18 @@ def quantize_e4m3(x):
     return codes, descale
 
 
+def quantize_e4m3_per_head(x):
+    """Per-(batch, head) amax quantisation of a [B, H, N, d] tensor.
+    Returns (uint8 codes, float32 descales of shape [B, H])."""
+    B, H = x.shape[0], x.shape[1]
+    codes = torch.empty(x.shape, dtype=torch.uint8)
+    descale = torch.empty((B, H), dtype=torch.float32)
+    for b in range(B):
+        for h in range(H):
+            codes[b, h], descale[b, h] = quantize_e4m3(x[b, h])
+    return codes, descale
+
+
 def attention_inputs(B, H, N, d, dtype="bf16", with_do=False,
                      seeds=(SEED_Q, SEED_K, SEED_V, SEED_DO)):
     """CPU tensors [B, H, N, d] for q, k, v (and do).  For ``e4m3`` the dict

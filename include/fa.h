@@ -94,6 +94,34 @@ int fa_fwd_fp8(const void* q8, const void* k8, const void* v8, void* o, float* l
                int B, int H, int N, int d, float scale, int causal, void* stream);
 
 /*
+ * Grouped-query forward: groups of H / H_kv query heads share one K/V head
+ * (the "GQA" of the "5.4 FlashAttention" page's heading; the arithmetic per query
+ * head is exactly fa_fwd's).  Query head h of batch b reads K/V head
+ * b*H_kv + h / (H / H_kv).
+ *
+ *   q, o : [B][H][N][d] bfloat16;  k, v : [B][H_kv][N][d] bfloat16;  lse [B][H][N].
+ *   dtype : FA_BF16.  d : 64 or 128.
+ * Errors: as fa_fwd; FA_ERR_INVALID_ARG also for H_kv < 1 or H % H_kv != 0;
+ * FA_ERR_UNSUPPORTED for FA_F32.
+ */
+int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+               int H_kv, int N, int d, float scale, int causal, int dtype, void* stream);
+
+/*
+ * FP8 forward with one dequantisation factor per (batch, head) instead of per
+ * tensor: finer scale factors ("Flash Attention V1/V2/V3演进", section V3增强).
+ * Element x of head (b, h) has the real value e4m3(x) * x_descale[b*H + h].
+ *
+ *   q_descale, k_descale, v_descale : DEVICE float32 arrays of B*H factors.
+ *   Other arguments as fa_fwd_fp8.
+ * Errors: as fa_fwd_fp8; FA_ERR_INVALID_ARG also for a null descale array.  The
+ * factors themselves are read on the device and not validated.
+ */
+int fa_fwd_fp8_per_head(const void* q8, const void* k8, const void* v8, void* o, float* lse,
+                        const float* q_descale, const float* k_descale, const float* v_descale,
+                        int B, int H, int N, int d, float scale, int causal, void* stream);
+
+/*
  * Bytes of device workspace that fa_bwd needs for these sizes: the per-row
  * delta_i = dO_i . O_i and the pre-scaled lse (float32, N rounded up to 128
  * per head) and the float32 dQ accumulator ([B][H][N rounded up to 128][d]).
