@@ -42,30 +42,39 @@
 namespace fa {
 namespace {
 
-constexpr int kD = 64;
 constexpr int kBlk = 128;            // keys per CTA, queries per inner step
-constexpr int kThreads = 512;
-constexpr int kQStages = 3;
-constexpr int kTile = kBlk * kD * 2;  // 16 KB bf16 tile (one 128-byte swizzle column)
 constexpr float kLog2e = 1.4426950408889634f;
 
-// shared memory map (offsets from a 1 KB aligned base)
-constexpr int kOffK = 0;
-constexpr int kOffV = kOffK + kTile;
-constexpr int kOffQ = kOffV + kTile;                     // kQStages
-constexpr int kOffDO = kOffQ + kQStages * kTile;         // kQStages
-constexpr int kOffDS = kOffDO + kQStages * kTile;        // 2 buffers x 32 KB (two 64-query columns)
-constexpr int kDSBytes = kBlk * kBlk * 2;
-constexpr int kOffL = kOffDS + 2 * kDSBytes;             // kQStages x 512 B
-constexpr int kOffDelta = kOffL + kQStages * kBlk * 4;   // kQStages x 512 B
-constexpr int kSmemBytes = kOffDelta + kQStages * kBlk * 4;
-constexpr int kSmemAlloc = kSmemBytes + 1024;
-
-constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 320, kColDQ = 384;
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kIdescSS = idesc_bf16(128, 128, false, false);  // S^T, dP^T
-constexpr uint32_t kIdescTS = idesc_bf16(128, kD, false, true);    // dV, dK
-constexpr uint32_t kIdescDQ = idesc_bf16(128, kD, true, true);     // dQ (A MN-major)
+// d = 64: dK, dV and dQ in one kernel (dQ partials through fp32 vector atomics).
+// d = 128: TMEM holds S^T, dP^T, dV and dK (4 x 128 columns) and nothing else, so
+// this kernel computes dK and dV only; bwd_dq_kernel computes dQ.
+template <int D>
+struct BwdCfg {
+    static constexpr bool kFusedDQ = (D == 64);
+    static constexpr int kThreads = kFusedDQ ? 512 : 384;
+    static constexpr int kQStages = kFusedDQ ? 3 : 2;
+    static constexpr int kChunks = D / 64;                    // 128-byte swizzle columns per row
+    static constexpr int kTile = kBlk * D * 2;                // bf16 128 x D tile
+    // shared memory map (offsets from a 1 KB aligned base)
+    static constexpr int kOffK = 0;
+    static constexpr int kOffV = kOffK + kTile;
+    static constexpr int kOffQ = kOffV + kTile;               // kQStages
+    static constexpr int kOffDO = kOffQ + kQStages * kTile;   // kQStages
+    static constexpr int kDSBytes = kBlk * kBlk * 2;
+    static constexpr int kOffDS = kOffDO + kQStages * kTile;  // fused: 2 x 32 KB (two 64-query columns)
+    static constexpr int kOffL = kOffDS + (kFusedDQ ? 2 * kDSBytes : 0);  // kQStages x 512 B
+    static constexpr int kOffDelta = kOffL + kQStages * kBlk * 4;          // kQStages x 512 B
+    static constexpr int kSmemBytes = kOffDelta + kQStages * kBlk * 4;
+    static constexpr int kSmemAlloc = kSmemBytes + 1024;
+    // TMEM columns
+    static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+    static constexpr uint32_t kColDQ = 384;                   // fused only
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kIdescSS = idesc_bf16(128, 128, false, false);  // S^T, dP^T
+    static constexpr uint32_t kIdescTS = idesc_bf16(128, D, false, true);     // dV, dK
+    static constexpr uint32_t kIdescDQ = idesc_bf16(128, D, true, true);      // dQ (A MN-major)
+};
+static_assert(BwdCfg<64>::kSmemAlloc <= 232448 && BwdCfg<128>::kSmemAlloc <= 232448, "smem");
 
 struct BwdArgs {
     const float* ws_delta;  // [BH][Np], negated: -delta_i
@@ -80,9 +89,10 @@ struct BwdArgs {
     DevCtl ctl;
 };
 
+template <int NQ>
 struct Bars {
     uint64_t kv_full;
-    uint64_t q_full[kQStages], q_empty[kQStages];
+    uint64_t q_full[NQ], q_empty[NQ];
     uint64_t s_full, dp_full, p_full, ds_full;
     uint64_t ds_empty[2];
     uint64_t dq_full[2], dq_free[2];
@@ -95,12 +105,20 @@ __device__ __forceinline__ void record_timeout(const DevCtl& ctl, volatile int* 
     atomicCAS(ctl.status, kDevOk, kDevTimeout);
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D>
+__global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const BwdArgs args) {
+    using C = BwdCfg<D>;
+    constexpr int kD = D, kQStages = C::kQStages, kTile = C::kTile, kChunks = C::kChunks;
+    constexpr int kOffK = C::kOffK, kOffV = C::kOffV, kOffQ = C::kOffQ, kOffDO = C::kOffDO;
+    constexpr int kOffDS = C::kOffDS, kDSBytes = C::kDSBytes, kOffL = C::kOffL, kOffDelta = C::kOffDelta;
+    constexpr uint32_t kColS = C::kColS, kColDP = C::kColDP, kColDV = C::kColDV, kColDK = C::kColDK;
+    constexpr uint32_t kColDQ = C::kColDQ, kTmemCols = C::kTmemCols;
+    constexpr uint32_t kIdescSS = C::kIdescSS, kIdescTS = C::kIdescTS, kIdescDQ = C::kIdescDQ;
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) Bars bars;
+    __shared__ __align__(8) Bars<kQStages> bars;
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
 
@@ -159,8 +177,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             const uint32_t kvf = smem_u32(&bars.kv_full);
             mbar_arrive_expect_tx(kvf, 2 * kTile);
-            tma_load_3d(sb + kOffK, &tm_k, kvf, 0, kvb * kBlk, bh);
-            tma_load_3d(sb + kOffV, &tm_v, kvf, 0, kvb * kBlk, bh);
+            for (int c = 0; c < kChunks; ++c) {  // 64-column swizzle chunks, 16 KB apart
+                tma_load_3d(sb + kOffK + c * 16384, &tm_k, kvf, 64 * c, kvb * kBlk, bh);
+                tma_load_3d(sb + kOffV + c * 16384, &tm_v, kvf, 64 * c, kvb * kBlk, bh);
+            }
             int issued = 0;
             bool ok = true;
             for (int i = 0; i < n_loc; ++i) {
@@ -173,8 +193,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const uint32_t qf = smem_u32(&bars.q_full[s]);
                 mbar_arrive_expect_tx(qf, 2 * kTile + 2 * kBlk * 4);
-                tma_load_3d(sb + kOffQ + s * kTile, &tm_q, qf, 0, qb * kBlk, bh);
-                tma_load_3d(sb + kOffDO + s * kTile, &tm_do, qf, 0, qb * kBlk, bh);
+                for (int c = 0; c < kChunks; ++c) {
+                    tma_load_3d(sb + kOffQ + s * kTile + c * 16384, &tm_q, qf, 64 * c, qb * kBlk, bh);
+                    tma_load_3d(sb + kOffDO + s * kTile + c * 16384, &tm_do, qf, 64 * c, qb * kBlk, bh);
+                }
                 const size_t row = static_cast<size_t>(bh) * Np + static_cast<size_t>(qb) * kBlk;
                 bulk_load(sb + kOffL + s * kBlk * 4, args.ws_lse2 + row, kBlk * 4, qf);
                 bulk_load(sb + kOffDelta + s * kBlk * 4, args.ws_delta + row, kBlk * 4, qf);
@@ -194,17 +216,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto issue_s = [&](int s) {  // S^T = K_j Q^T into columns 0-127
                 const uint32_t sQ = sb + kOffQ + s * kTile;
 #pragma unroll
-                for (int kk = 0; kk < kD / 16; ++kk)
-                    mma_bf16_ss(tmem + kColS, sdesc_sw128(sK + 32 * kk, 16, 1024),
-                                sdesc_sw128(sQ + 32 * kk, 16, 1024), kIdescSS, kk > 0);
+                for (int kk = 0; kk < kD / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                    mma_bf16_ss(tmem + kColS, sdesc_sw128(sK + off, 16, 1024),
+                                sdesc_sw128(sQ + off, 16, 1024), kIdescSS, kk > 0);
+                }
                 mma_commit(smem_u32(&bars.s_full));
             };
             auto issue_dp = [&](int s) {  // dP^T = V_j dO^T into columns 128-255
                 const uint32_t sDO = sb + kOffDO + s * kTile;
 #pragma unroll
-                for (int kk = 0; kk < kD / 16; ++kk)
-                    mma_bf16_ss(tmem + kColDP, sdesc_sw128(sV + 32 * kk, 16, 1024),
-                                sdesc_sw128(sDO + 32 * kk, 16, 1024), kIdescSS, kk > 0);
+                for (int kk = 0; kk < kD / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                    mma_bf16_ss(tmem + kColDP, sdesc_sw128(sV + off, 16, 1024),
+                                sdesc_sw128(sDO + off, 16, 1024), kIdescSS, kk > 0);
+                }
                 mma_commit(smem_u32(&bars.dp_full));
             };
             bool ok = mbar_wait(smem_u32(&bars.kv_full), 0, lim, &abort_flag);
@@ -244,20 +270,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 sdesc_sw128(sQ + 2048 * kk, 16384, 1024), kIdescTS, (i > 0) || (kk > 0));
                 mma_commit(smem_u32(&bars.q_empty[s]));  // Q_i, dO_i, lse_i, delta_i consumed
                 if (more) issue_dp(s1);
-                // dQ_i = dS_i K_j into TMEM buffer i % 2
-                const int b = i & 1;
-                if (i >= 2) {
-                    ok = mbar_wait(smem_u32(&bars.dq_free[b]), ((i >> 1) & 1) ^ 1, lim, &abort_flag);
-                    if (!ok) break;
-                    tc_fence_after();
-                }
-                const uint32_t sDS = sb + kOffDS + b * kDSBytes;
+                if constexpr (C::kFusedDQ) {
+                    // dQ_i = dS_i K_j into TMEM buffer i % 2
+                    const int b = i & 1;
+                    if (i >= 2) {
+                        ok = mbar_wait(smem_u32(&bars.dq_free[b]), ((i >> 1) & 1) ^ 1, lim, &abort_flag);
+                        if (!ok) break;
+                        tc_fence_after();
+                    }
+                    const uint32_t sDS = sb + kOffDS + b * kDSBytes;
 #pragma unroll
-                for (int kk = 0; kk < kBlk / 16; ++kk)
-                    mma_bf16_ss(tmem + kColDQ + 64 * b, sdesc_sw128(sDS + 2048 * kk, 16384, 1024),
-                                sdesc_sw128(sK + 2048 * kk, 16384, 1024), kIdescDQ, kk > 0);
-                mma_commit(smem_u32(&bars.dq_full[b]));
-                mma_commit(smem_u32(&bars.ds_empty[b]));
+                    for (int kk = 0; kk < kBlk / 16; ++kk)
+                        mma_bf16_ss(tmem + kColDQ + 64 * b, sdesc_sw128(sDS + 2048 * kk, 16384, 1024),
+                                    sdesc_sw128(sK + 2048 * kk, 16384, 1024), kIdescDQ, kk > 0);
+                    mma_commit(smem_u32(&bars.dq_full[b]));
+                    mma_commit(smem_u32(&bars.ds_empty[b]));
+                }
             }
             if (ok) mma_commit(smem_u32(&bars.all_done));
             if (!ok) record_timeout(args.ctl, &abort_flag);
@@ -266,6 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait(smem_u32(&bars.drain), 0, kDrainWaitNs, &never);
         }
     } else if (warp >= 4 && warp < 12) {
+        static_assert(C::kThreads >= 384, "P/dS warpgroups are warps 4-11");
         // ================================================================ P / dS warpgroups
         const int half = (warp - 4) / 4;          // query columns 64*half .. 64*half+63
         const int wq = warp % 4;
@@ -314,7 +343,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // dS^T = P^T o (dP^T - delta)
             const int b = i & 1;
             ok = mbar_wait(smem_u32(&bars.dp_full), i & 1, lim, &abort_flag);
-            if (ok && i >= 2) ok = mbar_wait(smem_u32(&bars.ds_empty[b]), ((i >> 1) & 1) ^ 1, lim, &abort_flag);
+            if (C::kFusedDQ && ok && i >= 2)
+                ok = mbar_wait(smem_u32(&bars.ds_empty[b]), ((i >> 1) & 1) ^ 1, lim, &abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
@@ -334,17 +364,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     w[x] = pack_bf16x2(ds.x, ds.y);
                 }
                 tmem_st16(lb + kColDP + 64 * half + 16 * h, w);
-                // queries 64*half + 32h .. +31 of this key row -> MN-major swizzled A tile
-                // for dQ: column `half`, row = key, 16-byte granule ((query % 64) / 8) ^ (key % 8)
+                if constexpr (C::kFusedDQ) {
+                    // queries 64*half + 32h .. +31 of this key row -> MN-major swizzled A tile
+                    // for dQ: column `half`, row = key, 16-byte granule ((query % 64) / 8) ^ (key % 8)
 #pragma unroll
-                for (int g4 = 0; g4 < 4; ++g4) {
-                    const int gran = (h * 4 + g4) ^ (key_in_blk & 7);
-                    *reinterpret_cast<uint4*>(dsrow + gran * 16) =
-                        make_uint4(w[4 * g4], w[4 * g4 + 1], w[4 * g4 + 2], w[4 * g4 + 3]);
+                    for (int g4 = 0; g4 < 4; ++g4) {
+                        const int gran = (h * 4 + g4) ^ (key_in_blk & 7);
+                        *reinterpret_cast<uint4*>(dsrow + gran * 16) =
+                            make_uint4(w[4 * g4], w[4 * g4 + 1], w[4 * g4 + 2], w[4 * g4 + 3]);
+                    }
                 }
             }
             tmem_st_wait();
-            fence_proxy_async_smem();
+            if constexpr (C::kFusedDQ) fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(smem_u32(&bars.ds_full));
         }
@@ -363,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t col = half ? kColDK : kColDV;
             uint16_t* out = static_cast<uint16_t*>(dst) + (static_cast<size_t>(bh) * N + key) * kD;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
+            for (int h = 0; h < kD / 32; ++h) {
                 uint32_t r[32];
                 tmem_ld32(lb + col + 32 * h, r);
                 if (key < N) {
@@ -378,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-    } else if (warp >= 12) {
+    } else if (C::kFusedDQ && warp >= 12) {
         // ================================================================ dQ drain
         const int wq = warp % 4;
         const int row_in_blk = wq * 32 + lane;
@@ -420,7 +452,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // -delta_i = -(dO_i . O_i) and -lse_i * log2(e) (rows past N: 0 and -inf, so
 // that recomputed P is exactly 0 there), dQ accumulator zeroed.  Both are stored
 // negated so the main kernel adds them with packed FMA/FADD.
-// 8 threads per row, each reading 16 bytes of O and dO.
+// D/8 threads per row, each reading 16 bytes of O and dO.
+template <int D>
 __global__ void bwd_prep_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dO,
                                 const float* __restrict__ lse, float* __restrict__ ws_delta,
                                 float* __restrict__ ws_lse2, float4* __restrict__ dq_acc, int BH,
@@ -428,13 +461,14 @@ __global__ void bwd_prep_kernel(const uint4* __restrict__ o, const uint4* __rest
     const size_t tid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const size_t nthreads = static_cast<size_t>(gridDim.x) * blockDim.x;
     const size_t rows = static_cast<size_t>(BH) * Np;
-    for (size_t base = tid; base < rows * 8; base += nthreads) {
-        const size_t r = base / 8;
-        const int part = static_cast<int>(base % 8);
+    constexpr int kT = D / 8;  // threads per row (8 or 16): the shuffles stay inside a warp
+    for (size_t base = tid; base < rows * kT; base += nthreads) {
+        const size_t r = base / kT;
+        const int part = static_cast<int>(base % kT);
         const int bh = static_cast<int>(r / Np), i = static_cast<int>(r % Np);
         float sum = 0.f;
         if (i < N) {
-            const size_t src = (static_cast<size_t>(bh) * N + i) * 8 + part;
+            const size_t src = (static_cast<size_t>(bh) * N + i) * kT + part;
             const uint4 a = o[src], b = dO[src];
             const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
@@ -446,6 +480,7 @@ __global__ void bwd_prep_kernel(const uint4* __restrict__ o, const uint4* __rest
         sum += __shfl_xor_sync(0xffffffffu, sum, 1);
         sum += __shfl_xor_sync(0xffffffffu, sum, 2);
         sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+        if (kT == 16) sum += __shfl_xor_sync(0xffffffffu, sum, 8);
         if (part == 0) {
             ws_delta[r] = -sum;
             ws_lse2[r] = (i < N) ? -lse[static_cast<size_t>(bh) * N + i] * kLog2e : -INFINITY;
@@ -455,12 +490,12 @@ __global__ void bwd_prep_kernel(const uint4* __restrict__ o, const uint4* __rest
     for (size_t x = tid; x < acc_vec4; x += nthreads) dq_acc[x] = z;
 }
 
-// dQ = bf16(scale * accumulator) for rows < N; 8 elements per thread.
+// dQ = bf16(scale * accumulator) for rows < N (d = 64); 8 elements per thread.
 __global__ void bwd_dq_convert_kernel(const float4* __restrict__ acc, uint4* __restrict__ dq,
                                       int N, int Np, size_t n_vec8, float scale) {
     const size_t tid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const size_t nthreads = static_cast<size_t>(gridDim.x) * blockDim.x;
-    constexpr int kVecPerRow = kD / 8;
+    constexpr int kVecPerRow = 64 / 8;
     for (size_t x = tid; x < n_vec8; x += nthreads) {
         const size_t row = x / kVecPerRow;  // row in [BH][N]
         const int part = static_cast<int>(x % kVecPerRow);
@@ -481,28 +516,30 @@ int grid_for(size_t work, int threads, int max_blocks) {
 }  // namespace
 
 size_t bwd_workspace_bytes(int BH, int N, int d) {
+    // -delta and -lse*log2(e) rows, plus the fp32 dQ accumulator when d = 64
     const size_t Np = static_cast<size_t>(round_up(N, kBlk));
-    return (2 * static_cast<size_t>(BH) * Np + static_cast<size_t>(BH) * Np * d) * sizeof(float);
+    const size_t acc = (d == 64) ? static_cast<size_t>(BH) * Np * d : 0;
+    return (2 * static_cast<size_t>(BH) * Np + acc) * sizeof(float);
 }
 
-int launch_bwd_sm103(const void* q, const void* k, const void* v, const void* o, const float* lse,
-                     const void* dO, void* dq, void* dk, void* dv, void* workspace, int BH, int N,
-                     int d, float scale, int causal, DevCtl ctl, cudaStream_t s) {
-    if (d != kD) return -1;
+namespace {
+
+template <int D>
+int launch_bwd_impl(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                    const void* dO, void* dq, void* dk, void* dv, void* workspace, int BH, int N,
+                    float scale, int causal, DevCtl ctl, cudaStream_t s) {
+    using C = BwdCfg<D>;
     const int Np = round_up(N, kBlk);
     float* ws = static_cast<float*>(workspace);
     float* ws_delta = ws;
     float* ws_lse2 = ws + static_cast<size_t>(BH) * Np;
-    float* dq_acc = ws + 2 * static_cast<size_t>(BH) * Np;
-    const size_t acc_vec4 = static_cast<size_t>(BH) * Np * kD / 4;
+    float* dq_acc = C::kFusedDQ ? ws + 2 * static_cast<size_t>(BH) * Np : nullptr;
+    const size_t acc_vec4 = C::kFusedDQ ? static_cast<size_t>(BH) * Np * D / 4 : 0;
 
-    int sms = 152;
-    {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    }
-    bwd_prep_kernel<<<grid_for(static_cast<size_t>(BH) * Np * 8, 256, sms * 8), 256, 0, s>>>(
+    int sms = 152, dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    bwd_prep_kernel<D><<<grid_for(static_cast<size_t>(BH) * Np * (D / 8), 256, sms * 8), 256, 0, s>>>(
         static_cast<const uint4*>(o), static_cast<const uint4*>(dO), lse, ws_delta, ws_lse2,
         reinterpret_cast<float4*>(dq_acc), BH, N, Np, acc_vec4);
     cudaError_t e = cudaGetLastError();
@@ -510,16 +547,15 @@ int launch_bwd_sm103(const void* q, const void* k, const void* v, const void* o,
 
     CUtensorMap tq, tk, tv, tdo;
     const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    int rc = make_map_3d(&tq, q, dt, 2, kD, N, BH, 64, kBlk);
-    if (rc == 0) rc = make_map_3d(&tk, k, dt, 2, kD, N, BH, 64, kBlk);
-    if (rc == 0) rc = make_map_3d(&tv, v, dt, 2, kD, N, BH, 64, kBlk);
-    if (rc == 0) rc = make_map_3d(&tdo, dO, dt, 2, kD, N, BH, 64, kBlk);
+    int rc = make_map_3d(&tq, q, dt, 2, D, N, BH, 64, kBlk);
+    if (rc == 0) rc = make_map_3d(&tk, k, dt, 2, D, N, BH, 64, kBlk);
+    if (rc == 0) rc = make_map_3d(&tv, v, dt, 2, D, N, BH, 64, kBlk);
+    if (rc == 0) rc = make_map_3d(&tdo, dO, dt, 2, D, N, BH, 64, kBlk);
     if (rc != 0) return rc;
     static uint64_t attr_set = 0;
-    int dev = 0;
-    cudaGetDevice(&dev);
     if (dev >= 64 || !(attr_set & (1ull << dev))) {
-        e = cudaFuncSetAttribute(bwd_main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+        e = cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 C::kSmemAlloc);
         if (e != cudaSuccess) return static_cast<int>(e);
         if (dev < 64) attr_set |= 1ull << dev;
     }
@@ -537,14 +573,33 @@ int launch_bwd_sm103(const void* q, const void* k, const void* v, const void* o,
     a.c_log2 = scale * kLog2e;
     a.scale = scale;
     a.ctl = ctl;
-    bwd_main_kernel<<<a.n_kv * BH, kThreads, kSmemAlloc, s>>>(tq, tk, tv, tdo, a);
+    bwd_main_kernel<D><<<a.n_kv * BH, C::kThreads, C::kSmemAlloc, s>>>(tq, tk, tv, tdo, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return static_cast<int>(e);
 
-    const size_t n_vec8 = static_cast<size_t>(BH) * N * kD / 8;
-    bwd_dq_convert_kernel<<<grid_for(n_vec8, 256, sms * 8), 256, 0, s>>>(
-        reinterpret_cast<const float4*>(dq_acc), static_cast<uint4*>(dq), N, Np, n_vec8, scale);
-    return static_cast<int>(cudaGetLastError());
+    if constexpr (C::kFusedDQ) {
+        const size_t n_vec8 = static_cast<size_t>(BH) * N * D / 8;
+        bwd_dq_convert_kernel<<<grid_for(n_vec8, 256, sms * 8), 256, 0, s>>>(
+            reinterpret_cast<const float4*>(dq_acc), static_cast<uint4*>(dq), N, Np, n_vec8, scale);
+        return static_cast<int>(cudaGetLastError());
+    } else {
+        // dQ by its own query-parallel kernel: recompute S and dP per query block
+        return launch_bwd_dq(q, k, v, dO, ws_lse2, ws_delta, dq, BH, N, D, scale, causal, ctl, s);
+    }
+}
+
+}  // namespace
+
+int launch_bwd_sm103(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                     const void* dO, void* dq, void* dk, void* dv, void* workspace, int BH, int N,
+                     int d, float scale, int causal, DevCtl ctl, cudaStream_t s) {
+    if (d == 64)
+        return launch_bwd_impl<64>(q, k, v, o, lse, dO, dq, dk, dv, workspace, BH, N, scale, causal,
+                                   ctl, s);
+    if (d == 128)
+        return launch_bwd_impl<128>(q, k, v, o, lse, dO, dq, dk, dv, workspace, BH, N, scale, causal,
+                                    ctl, s);
+    return -1;
 }
 
 }  // namespace fa

@@ -201,7 +201,7 @@ __attribute__((visibility("default"))) int fa_bwd(const void* q, const void* k, 
         return FA_ERR_INVALID_ARG;
     if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
     if (dtype != FA_F32 && dtype != FA_BF16 && dtype != FA_E4M3) return FA_ERR_INVALID_ARG;
-    if (dtype != FA_BF16 || d != 64) return FA_ERR_UNSUPPORTED;
+    if (dtype != FA_BF16 || (d != 64 && d != 128)) return FA_ERR_UNSUPPORTED;
     if (workspace_bytes < bwd_workspace_bytes(B * H, N, d)) return FA_ERR_INVALID_ARG;
     int err = FA_OK;
     int* st = status_word(&err);

@@ -124,7 +124,8 @@ int fa_fwd_fp8_per_head(const void* q8, const void* k8, const void* v8, void* o,
 /*
  * Bytes of device workspace that fa_bwd needs for these sizes: the per-row
  * delta_i = dO_i . O_i and the pre-scaled lse (float32, N rounded up to 128
- * per head) and the float32 dQ accumulator ([B][H][N rounded up to 128][d]).
+ * per head), plus for d = 64 the float32 dQ accumulator
+ * ([B][H][N rounded up to 128][d]).
  * Returns 0 for invalid sizes.
  */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);
@@ -142,7 +143,9 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d);
  *                    owned by the caller; its contents on entry do not matter
  *                    and on return are unspecified.  Calls that overlap in time
  *                    must not share one workspace.
- *   dtype          : FA_BF16.   d : 64.
+ *   dtype          : FA_BF16.   d : 64 or 128 (d = 64 accumulates dQ with fp32
+ *                    atomics in the workspace; d = 128 computes dQ in a second,
+ *                    query-parallel kernel, and its workspace holds no accumulator).
  *   causal         : 0, or 1 for the causal mask of the forward (key j reaches
  *                    only queries i >= j; lse must come from a causal forward).
  * Errors: FA_ERR_INVALID_ARG (null/misaligned pointers, workspace too small,

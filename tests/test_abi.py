@@ -57,6 +57,8 @@ def test_workspace_size(L):
     # delta + lse2 ([BH][Np]) and the fp32 dQ accumulator ([BH][Np][d]), Np = ceil128(N)
     B, H, N, d = 4, 16, 2048, 64
     assert fa.fa_bwd_workspace_size(B, H, N, d) == (2 * B * H * N + B * H * N * d) * 4
+    # d = 128 computes dQ without an accumulator: only the two row vectors
+    assert fa.fa_bwd_workspace_size(B, H, N, 128) == 2 * B * H * N * 4
     Np = 256
     assert fa.fa_bwd_workspace_size(1, 3, 130, 64) == (2 * 3 * Np + 3 * Np * 64) * 4
     assert fa.fa_bwd_workspace_size(0, 1, 1, 64) == 0
@@ -107,4 +109,4 @@ def test_bwd_argument_errors(L):
     assert b(ws_bytes=ws - 4) == 1
     assert b(dtype=9) == 1
     assert b(dtype=0) == 2
-    assert b(d=128) == 2
+    assert b(d=96) == 2

@@ -27,9 +27,10 @@ def run_bwd(dev, scale, causal=False):
 
 @pytest.mark.parametrize("N", [1, 17, 128, 130, 255, 384, 700])
 @pytest.mark.parametrize("causal", [False, True])
-def test_bwd_small(N, causal):
-    x, dev = device_inputs(1, 2, N, 64, "bf16", with_do=True)
-    s = scale_for(64)
+@pytest.mark.parametrize("d", [64, 128])
+def test_bwd_small(N, causal, d):
+    x, dev = device_inputs(1, 2, N, d, "bf16", with_do=True)
+    s = scale_for(d)
     got = run_bwd(dev, s, causal)
     ref = oracle.attn_bwd(f64(x["q"]), f64(x["k"]), f64(x["v"]), f64(x["do"]), s, causal)
     for name, g, r in zip(("dq", "dk", "dv"), got, ref):
@@ -79,3 +80,18 @@ def test_bwd_causal_b4_h16_n2048_d64_sampled_heads():
     # query 0 sees only key 0: O_0 = V_0, so dS_00 = dO_0 . (V_0 - O_0) = 0 and dQ_0 = 0
     assert np.isfinite(dv).all() and np.isfinite(dq).all()
     assert np.abs(dq[:, :, 0]).max() <= 1e-2
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_d128_b1_h8_n4096_sampled_heads(causal):
+    # d = 128: key-parallel dK/dV kernel plus the query-parallel dQ kernel
+    B, H, N, d = 1, 8, 4096, 128
+    x, dev = device_inputs(B, H, N, d, "bf16", with_do=True)
+    s = scale_for(d)
+    dq, dk, dv = (f64(t) for t in run_bwd(dev, s, causal))
+    for h in (0, 5):
+        ref = oracle.attn_bwd(f64(x["q"][0, h]), f64(x["k"][0, h]), f64(x["v"][0, h]),
+                              f64(x["do"][0, h]), s, causal)
+        for name, g, r in zip(("dq", "dk", "dv"), (dq[0, h], dk[0, h], dv[0, h]), ref):
+            assert max_err(g, r) <= TOL_BF16_GRAD, name
+    np.testing.assert_allclose(dv.sum(2), f64(x["do"]).sum(2), atol=0.25)
