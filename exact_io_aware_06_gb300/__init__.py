@@ -55,6 +55,9 @@ def lib():
         L.fa_bwd_workspace_size.argtypes = [i, i, i, i]
         L.fa_bwd_workspace_size.restype = sz
         L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, f, i, i, vp]
+        L.fa_bwd_gqa.restype = i
+        L.fa_bwd_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, f, i, i,
+                                 vp]
         L.fa_bwd.restype = i
         L.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
         L.fa_bwd_noalloc.restype = i
@@ -151,6 +154,17 @@ def fa_bwd(q, k, v, o, lse, do, dq, dk, dv, workspace, scale, causal, dtype, str
                         int(bool(causal)), int(dtype), _stream(stream)), "fa_bwd")
 
 
+def fa_bwd_gqa(q, k, v, o, lse, do, dq, dk, dv, workspace, scale, causal, dtype, stream=None):
+    """Grouped-query backward: q, o, do, dq [B, H, N, d]; k, v, dk, dv [B, H_kv, N, d]."""
+    B, H, N, d = _shape(q)
+    H_kv = _shape(k)[1]
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(lib().fa_bwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq),
+                            _ptr(dk), _ptr(dv), _ptr(workspace), nbytes, B, H, H_kv, N, d,
+                            float(scale), int(bool(causal)), int(dtype), _stream(stream)),
+           "fa_bwd_gqa")
+
+
 def fa_bwd_noalloc(q, k, v, o, lse, do, dq, dk, dv, scale, causal, dtype, stream=None):
     """fa_bwd with the library's built-in scratch (no workspace, no allocation).
     For callers that cannot allocate device memory at call time; calls that
@@ -182,7 +196,9 @@ def attention_forward(q, k, v, scale=None, causal=False, stream=None):
     B, H, N, d = _shape(q)
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    fa_fwd(q, k, v, o, lse, 1.0 / math.sqrt(d) if scale is None else scale, causal, dtype, stream)
+    # k, v with fewer heads than q: grouped-query attention
+    fn = fa_fwd if _shape(k)[1] == H else fa_fwd_gqa
+    fn(q, k, v, o, lse, 1.0 / math.sqrt(d) if scale is None else scale, causal, dtype, stream)
     return o, lse
 
 
@@ -191,6 +207,8 @@ def attention_backward(q, k, v, o, lse, do, scale=None, causal=False, stream=Non
     B, H, N, d = _shape(q)
     ws = torch.empty(fa_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    fa_bwd(q, k, v, o, lse, do, dq, dk, dv, ws, 1.0 / math.sqrt(d) if scale is None else scale,
-           causal, FA_BF16, stream)
+    # k, v with fewer heads than q: grouped-query attention
+    fn = fa_bwd if _shape(k)[1] == H else fa_bwd_gqa
+    fn(q, k, v, o, lse, do, dq, dk, dv, ws, 1.0 / math.sqrt(d) if scale is None else scale,
+       causal, FA_BF16, stream)
     return dq, dk, dv

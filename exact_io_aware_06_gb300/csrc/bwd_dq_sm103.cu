@@ -47,7 +47,8 @@ struct DqArgs {
     const float* ws_nlse2;   // [BH][Np]: -lse * log2(e) (-inf on pad rows)
     const float* ws_ndelta;  // [BH][Np]: -delta
     void* dq;
-    int N, Np, n_q, BH;
+    int N, Np, n_q, BH;      // BH: query heads (B * H)
+    int H, H_kv;             // query heads and K/V heads per batch; H_kv divides H
     int causal;
     float c_log2;            // scale * log2(e)
     float scale;
@@ -82,6 +83,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int bh = args.causal ? static_cast<int>(blockIdx.x % args.BH) : static_cast<int>(blockIdx.x / args.n_q);
     const int qb = args.causal ? args.n_q - 1 - static_cast<int>(blockIdx.x / args.BH)
                                : static_cast<int>(blockIdx.x % args.n_q);
+    // grouped-query attention: query head bh reads K/V head bh_kv of its group
+    const int bh_kv = (bh / args.H) * args.H_kv + (bh % args.H) / (args.H / args.H_kv);
     const int N = args.N, Np = args.Np;
     const int n_kv = args.causal ? qb + 1 : Np / kBlk;  // key blocks this query block meets
     const uint64_t lim = args.ctl.wait_ns;
@@ -135,8 +138,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t kf = smem_u32(&bars.kv_full[s]);
                 mbar_arrive_expect_tx(kf, 2 * C::kTile);
                 for (int c = 0; c < C::kChunks; ++c) {
-                    tma_load_3d(sb + C::kOffK + s * C::kTile + c * 16384, &tm_k, kf, 64 * c, j * kBlk, bh);
-                    tma_load_3d(sb + C::kOffV + s * C::kTile + c * 16384, &tm_v, kf, 64 * c, j * kBlk, bh);
+                    tma_load_3d(sb + C::kOffK + s * C::kTile + c * 16384, &tm_k, kf, 64 * c, j * kBlk, bh_kv);
+                    tma_load_3d(sb + C::kOffV + s * C::kTile + c * 16384, &tm_v, kf, 64 * c, j * kBlk, bh_kv);
                 }
                 issued = j + 1;
             }
@@ -286,15 +289,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 int launch_bwd_dq(const void* q, const void* k, const void* v, const void* dO,
-                  const float* ws_nlse2, const float* ws_ndelta, void* dq, int BH, int N, int d,
-                  float scale, int causal, DevCtl ctl, cudaStream_t s) {
+                  const float* ws_nlse2, const float* ws_ndelta, void* dq, int B, int H, int H_kv,
+                  int N, int d, float scale, int causal, DevCtl ctl, cudaStream_t s) {
     if (d != 128) return -1;
+    const int BH = B * H, BH_kv = B * H_kv;
     using C = DqCfg<128>;
     CUtensorMap tq, tk, tv, tdo;
     const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     int rc = make_map_3d(&tq, q, dt, 2, 128, N, BH, 64, kBlk);
-    if (rc == 0) rc = make_map_3d(&tk, k, dt, 2, 128, N, BH, 64, kBlk);
-    if (rc == 0) rc = make_map_3d(&tv, v, dt, 2, 128, N, BH, 64, kBlk);
+    if (rc == 0) rc = make_map_3d(&tk, k, dt, 2, 128, N, BH_kv, 64, kBlk);
+    if (rc == 0) rc = make_map_3d(&tv, v, dt, 2, 128, N, BH_kv, 64, kBlk);
     if (rc == 0) rc = make_map_3d(&tdo, dO, dt, 2, 128, N, BH, 64, kBlk);
     if (rc != 0) return rc;
     static uint64_t attr_set = 0;
@@ -314,6 +318,8 @@ int launch_bwd_dq(const void* q, const void* k, const void* v, const void* dO,
     a.Np = round_up(N, kBlk);
     a.n_q = a.Np / kBlk;
     a.BH = BH;
+    a.H = H;
+    a.H_kv = H_kv;
     a.causal = causal ? 1 : 0;
     a.c_log2 = scale * 1.4426950408889634f;
     a.scale = scale;

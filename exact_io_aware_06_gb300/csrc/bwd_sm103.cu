@@ -82,7 +82,8 @@ struct BwdArgs {
     float* dq_acc;          // [BH][Np][d]
     void* dk;
     void* dv;
-    int N, Np, n_kv, BH;
+    int N, Np, n_kv, BH;    // BH: K/V heads (B * H_kv), the grid's head count
+    int H, H_kv;            // query heads and K/V heads per batch; H_kv divides H
     int causal;             // 1: key j only reaches queries i >= j
     float c_log2;           // scale * log2(e)
     float scale;
@@ -131,10 +132,17 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const int N = args.N, Np = args.Np;
     const int n_q = Np / kBlk;
     // query blocks this key block meets: all of them, or (causal) blocks kvb..n_q-1.
-    // Loops run over the local index i (barrier phases, stages, buffers); the query
-    // block itself is i0 + i.
+    // Loops run over a sweep index (barrier phases, stages, buffers); q_blk() and
+    // q_head() below map it to the query block and query head.
     const int i0 = args.causal ? kvb : 0;
     const int n_loc = n_q - i0;
+    // grouped-query attention: this K/V head (bh) serves G query heads, and its dK, dV
+    // sum over all of them.  The sweep runs over it = g * n_loc + i for every query
+    // head g of the group; with H_kv = H it is the plain sweep.
+    const int G = args.H / args.H_kv;
+    const int n_it = G * n_loc;
+    auto q_head = [&](int it) { return (bh / args.H_kv) * args.H + (bh % args.H_kv) * G + it / n_loc; };
+    auto q_blk = [&](int it) { return i0 + it % n_loc; };
     const uint64_t lim = args.ctl.wait_ns;
 
     if (threadIdx.x == 0) {
@@ -183,9 +191,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             }
             int issued = 0;
             bool ok = true;
-            for (int i = 0; i < n_loc; ++i) {
+            for (int i = 0; i < n_it; ++i) {
                 const int s = i % kQStages;
-                const int qb = i0 + i;
+                const int qb = q_blk(i), qh = q_head(i);
                 if (i >= kQStages &&
                     !mbar_wait(smem_u32(&bars.q_empty[s]), ((i / kQStages) & 1) ^ 1, lim, &abort_flag)) {
                     ok = false;
@@ -194,10 +202,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                 const uint32_t qf = smem_u32(&bars.q_full[s]);
                 mbar_arrive_expect_tx(qf, 2 * kTile + 2 * kBlk * 4);
                 for (int c = 0; c < kChunks; ++c) {
-                    tma_load_3d(sb + kOffQ + s * kTile + c * 16384, &tm_q, qf, 64 * c, qb * kBlk, bh);
-                    tma_load_3d(sb + kOffDO + s * kTile + c * 16384, &tm_do, qf, 64 * c, qb * kBlk, bh);
+                    tma_load_3d(sb + kOffQ + s * kTile + c * 16384, &tm_q, qf, 64 * c, qb * kBlk, qh);
+                    tma_load_3d(sb + kOffDO + s * kTile + c * 16384, &tm_do, qf, 64 * c, qb * kBlk, qh);
                 }
-                const size_t row = static_cast<size_t>(bh) * Np + static_cast<size_t>(qb) * kBlk;
+                const size_t row = static_cast<size_t>(qh) * Np + static_cast<size_t>(qb) * kBlk;
                 bulk_load(sb + kOffL + s * kBlk * 4, args.ws_lse2 + row, kBlk * 4, qf);
                 bulk_load(sb + kOffDelta + s * kBlk * 4, args.ws_delta + row, kBlk * 4, qf);
                 issued = i + 1;
@@ -240,10 +248,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                 issue_s(0);
                 issue_dp(0);
             }
-            for (int i = 0; i < n_loc && ok; ++i) {
+            for (int i = 0; i < n_it && ok; ++i) {
                 const int s = i % kQStages;
                 const int s1 = (i + 1) % kQStages;
-                const bool more = i + 1 < n_loc;
+                const bool more = i + 1 < n_it;
                 const uint32_t sQ = sb + kOffQ + s * kTile, sDO = sb + kOffDO + s * kTile;
                 // dV += P^T dO_i
                 ok = mbar_wait(smem_u32(&bars.p_full), i & 1, lim, &abort_flag);
@@ -302,10 +310,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         const uint32_t lb = tmem + (static_cast<uint32_t>(wq * 32) << 16);
         const float2 c2 = make_float2(args.c_log2, args.c_log2);
         bool ok = true;
-        for (int i = 0; i < n_loc; ++i) {
+        for (int i = 0; i < n_it; ++i) {
             const int s = i % kQStages;
             // causal diagonal block: key k only reaches queries q >= k of the block
-            const bool diag = args.causal && (i0 + i == kvb);
+            const bool diag = args.causal && (q_blk(i) == kvb);
             ok = mbar_wait(smem_u32(&bars.q_full[s]), (i / kQStages) & 1, lim, &abort_flag);
             if (ok) ok = mbar_wait(smem_u32(&bars.s_full), i & 1, lim, &abort_flag);
             ok = __all_sync(0xffffffffu, ok);
@@ -416,7 +424,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         const int row_in_blk = wq * 32 + lane;
         const uint32_t lb = tmem + (static_cast<uint32_t>(wq * 32) << 16);
         bool ok = true;
-        for (int i = 0; i < n_loc; ++i) {
+        for (int i = 0; i < n_it; ++i) {
             const int b = i & 1;
             ok = mbar_wait(smem_u32(&bars.dq_full[b]), (i >> 1) & 1, lim, &abort_flag);
             ok = __all_sync(0xffffffffu, ok);
@@ -427,7 +435,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             tmem_ld32(lb + kColDQ + 64 * b + 32, r[1]);
             tc_fence_before();
             mbar_arrive(smem_u32(&bars.dq_free[b]));
-            float* acc = args.dq_acc + (static_cast<size_t>(bh) * Np + static_cast<size_t>(i0 + i) * kBlk + row_in_blk) * kD;
+            float* acc = args.dq_acc +
+                         (static_cast<size_t>(q_head(i)) * Np + static_cast<size_t>(q_blk(i)) * kBlk + row_in_blk) * kD;
 #pragma unroll
             for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -526,9 +535,10 @@ namespace {
 
 template <int D>
 int launch_bwd_impl(const void* q, const void* k, const void* v, const void* o, const float* lse,
-                    const void* dO, void* dq, void* dk, void* dv, void* workspace, int BH, int N,
-                    float scale, int causal, DevCtl ctl, cudaStream_t s) {
+                    const void* dO, void* dq, void* dk, void* dv, void* workspace, int B, int H,
+                    int H_kv, int N, float scale, int causal, DevCtl ctl, cudaStream_t s) {
     using C = BwdCfg<D>;
+    const int BH = B * H, BH_kv = B * H_kv;  // query heads; K/V heads
     const int Np = round_up(N, kBlk);
     float* ws = static_cast<float*>(workspace);
     float* ws_delta = ws;
@@ -548,8 +558,8 @@ int launch_bwd_impl(const void* q, const void* k, const void* v, const void* o, 
     CUtensorMap tq, tk, tv, tdo;
     const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     int rc = make_map_3d(&tq, q, dt, 2, D, N, BH, 64, kBlk);
-    if (rc == 0) rc = make_map_3d(&tk, k, dt, 2, D, N, BH, 64, kBlk);
-    if (rc == 0) rc = make_map_3d(&tv, v, dt, 2, D, N, BH, 64, kBlk);
+    if (rc == 0) rc = make_map_3d(&tk, k, dt, 2, D, N, BH_kv, 64, kBlk);
+    if (rc == 0) rc = make_map_3d(&tv, v, dt, 2, D, N, BH_kv, 64, kBlk);
     if (rc == 0) rc = make_map_3d(&tdo, dO, dt, 2, D, N, BH, 64, kBlk);
     if (rc != 0) return rc;
     static uint64_t attr_set = 0;
@@ -568,12 +578,14 @@ int launch_bwd_impl(const void* q, const void* k, const void* v, const void* o, 
     a.N = N;
     a.Np = Np;
     a.n_kv = Np / kBlk;
-    a.BH = BH;
+    a.BH = BH_kv;
+    a.H = H;
+    a.H_kv = H_kv;
     a.causal = causal ? 1 : 0;
     a.c_log2 = scale * kLog2e;
     a.scale = scale;
     a.ctl = ctl;
-    bwd_main_kernel<D><<<a.n_kv * BH, C::kThreads, C::kSmemAlloc, s>>>(tq, tk, tv, tdo, a);
+    bwd_main_kernel<D><<<a.n_kv * BH_kv, C::kThreads, C::kSmemAlloc, s>>>(tq, tk, tv, tdo, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return static_cast<int>(e);
 
@@ -584,21 +596,22 @@ int launch_bwd_impl(const void* q, const void* k, const void* v, const void* o, 
         return static_cast<int>(cudaGetLastError());
     } else {
         // dQ by its own query-parallel kernel: recompute S and dP per query block
-        return launch_bwd_dq(q, k, v, dO, ws_lse2, ws_delta, dq, BH, N, D, scale, causal, ctl, s);
+        return launch_bwd_dq(q, k, v, dO, ws_lse2, ws_delta, dq, B, H, H_kv, N, D, scale, causal,
+                             ctl, s);
     }
 }
 
 }  // namespace
 
 int launch_bwd_sm103(const void* q, const void* k, const void* v, const void* o, const float* lse,
-                     const void* dO, void* dq, void* dk, void* dv, void* workspace, int BH, int N,
-                     int d, float scale, int causal, DevCtl ctl, cudaStream_t s) {
+                     const void* dO, void* dq, void* dk, void* dv, void* workspace, int B, int H,
+                     int H_kv, int N, int d, float scale, int causal, DevCtl ctl, cudaStream_t s) {
     if (d == 64)
-        return launch_bwd_impl<64>(q, k, v, o, lse, dO, dq, dk, dv, workspace, BH, N, scale, causal,
-                                   ctl, s);
+        return launch_bwd_impl<64>(q, k, v, o, lse, dO, dq, dk, dv, workspace, B, H, H_kv, N, scale,
+                                   causal, ctl, s);
     if (d == 128)
-        return launch_bwd_impl<128>(q, k, v, o, lse, dO, dq, dk, dv, workspace, BH, N, scale, causal,
-                                    ctl, s);
+        return launch_bwd_impl<128>(q, k, v, o, lse, dO, dq, dk, dv, workspace, B, H, H_kv, N,
+                                    scale, causal, ctl, s);
     return -1;
 }
 

@@ -185,12 +185,13 @@ __attribute__((visibility("default"))) size_t fa_bwd_workspace_size(int B, int H
     return bwd_workspace_bytes(B * H, N, d);
 }
 
-__attribute__((visibility("default"))) int fa_bwd(const void* q, const void* k, const void* v,
-                                                  const void* o, const float* lse, const void* dO,
-                                                  void* dq, void* dk, void* dv, void* workspace,
-                                                  size_t workspace_bytes, int B, int H, int N,
-                                                  int d, float scale, int causal, int dtype,
-                                                  void* stream) {
+__attribute__((visibility("default"))) int fa_bwd_gqa(const void* q, const void* k,
+                                                      const void* v, const void* o,
+                                                      const float* lse, const void* dO, void* dq,
+                                                      void* dk, void* dv, void* workspace,
+                                                      size_t workspace_bytes, int B, int H,
+                                                      int H_kv, int N, int d, float scale,
+                                                      int causal, int dtype, void* stream) {
     int rc = check_common(q, k, v, o, lse, B, H, N);
     if (rc != FA_OK) return rc;
     if (lse == nullptr || dO == nullptr || dq == nullptr || dk == nullptr || dv == nullptr ||
@@ -199,7 +200,7 @@ __attribute__((visibility("default"))) int fa_bwd(const void* q, const void* k, 
     if (!aligned16(dO) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
         !aligned16(workspace))
         return FA_ERR_INVALID_ARG;
-    if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || H_kv < 1 || H % H_kv != 0) return FA_ERR_INVALID_ARG;
     if (dtype != FA_F32 && dtype != FA_BF16 && dtype != FA_E4M3) return FA_ERR_INVALID_ARG;
     if (dtype != FA_BF16 || (d != 64 && d != 128)) return FA_ERR_UNSUPPORTED;
     if (workspace_bytes < bwd_workspace_bytes(B * H, N, d)) return FA_ERR_INVALID_ARG;
@@ -207,8 +208,18 @@ __attribute__((visibility("default"))) int fa_bwd(const void* q, const void* k, 
     int* st = status_word(&err);
     if (st == nullptr) return err;
     DevCtl ctl{st, g_wait_ns.load()};
-    return from_cuda(launch_bwd_sm103(q, k, v, o, lse, dO, dq, dk, dv, workspace, B * H, N, d,
+    return from_cuda(launch_bwd_sm103(q, k, v, o, lse, dO, dq, dk, dv, workspace, B, H, H_kv, N, d,
                                       scale, causal ? 1 : 0, ctl, static_cast<cudaStream_t>(stream)));
+}
+
+__attribute__((visibility("default"))) int fa_bwd(const void* q, const void* k, const void* v,
+                                                  const void* o, const float* lse, const void* dO,
+                                                  void* dq, void* dk, void* dv, void* workspace,
+                                                  size_t workspace_bytes, int B, int H, int N,
+                                                  int d, float scale, int causal, int dtype,
+                                                  void* stream) {
+    return fa_bwd_gqa(q, k, v, o, lse, dO, dq, dk, dv, workspace, workspace_bytes, B, H, H, N, d,
+                      scale, causal, dtype, stream);
 }
 
 __attribute__((visibility("default"))) int fa_last_device_error(void* stream) {

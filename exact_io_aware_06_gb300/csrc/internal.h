@@ -35,21 +35,23 @@ int launch_fwd_sm103(const void* q, const void* k, const void* v, void* o, float
                      cudaStream_t s);
 
 // Backward pieces.  Workspace layout (all float32, Np = N rounded up to 128):
-//   [0, BH*Np)            -delta_i = -(dO_i . O_i)
+//   [0, BH*Np)            -delta_i  (BH = B*H query heads) = -(dO_i . O_i)
 //   [BH*Np, 2*BH*Np)      -lse_i * log2(e)   (both negated for packed FMA/FADD use)
 //   [2*BH*Np, ...)        dQ accumulator [BH][Np][d] (d = 64 only; d = 128 computes dQ
 //                         in a separate kernel without an accumulator)
 size_t bwd_workspace_bytes(int BH, int N, int d);
+// Q, O, dO, lse, dQ have B*H heads; K, V, dK, dV have B*H_kv heads (H_kv divides H;
+// each K/V head's gradients sum over the H/H_kv query heads that share it).
 int launch_bwd_sm103(const void* q, const void* k, const void* v, const void* o, const float* lse,
-                     const void* dO, void* dq, void* dk, void* dv, void* workspace, int BH, int N,
-                     int d, float scale, int causal, DevCtl ctl, cudaStream_t s);
+                     const void* dO, void* dq, void* dk, void* dv, void* workspace, int B, int H,
+                     int H_kv, int N, int d, float scale, int causal, DevCtl ctl, cudaStream_t s);
 
 // dQ for d = 128 by a query-parallel kernel (recomputes S and dP per query block,
 // accumulates dQ in TMEM, writes bf16 dQ = scale * dS K directly).  ws_nlse2 and
-// ws_ndelta are the backward workspace's negated rows ([BH][Np] each).
+// ws_ndelta are the backward workspace's negated rows ([B*H][Np] each).
 int launch_bwd_dq(const void* q, const void* k, const void* v, const void* dO,
-                  const float* ws_nlse2, const float* ws_ndelta, void* dq, int BH, int N, int d,
-                  float scale, int causal, DevCtl ctl, cudaStream_t s);
+                  const float* ws_nlse2, const float* ws_ndelta, void* dq, int B, int H, int H_kv,
+                  int N, int d, float scale, int causal, DevCtl ctl, cudaStream_t s);
 
 // A kernel that waits on a barrier nobody arrives at, with the bounded wait;
 // it must record kDevTimeout and return.

@@ -158,6 +158,28 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
            int dtype, void* stream);
 
 /*
+ * Grouped-query backward, the gradient of fa_fwd_gqa: query head h of batch b
+ * reads K/V head b*H_kv + h / (H / H_kv), so each K/V head's dK and dV are the
+ * sums of the per-query-head gradients over the H / H_kv query heads sharing it
+ * (the chain rule through the shared operand; the pages give the forward
+ * grouping under "5.4 FlashAttention" and the per-head backward in
+ * "FlashAttention-1", 10.2.4).  With H_kv = H this is fa_bwd.
+ *
+ *   q, o, dO : [B][H][N][d] bfloat16;  lse [B][H][N] float32 (from fa_fwd_gqa).
+ *   k, v     : [B][H_kv][N][d] bfloat16.
+ *   dq       : [B][H][N][d] bfloat16, written.
+ *   dk, dv   : [B][H_kv][N][d] bfloat16, written (the group sums, accumulated
+ *              in fp32 on chip and rounded once).
+ *   workspace: at least fa_bwd_workspace_size(B, H, N, d) bytes (query heads).
+ *   Other arguments as fa_bwd.
+ * Errors: as fa_bwd; FA_ERR_INVALID_ARG also for H_kv < 1 or H % H_kv != 0.
+ */
+int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const float* lse,
+               const void* dO, void* dq, void* dk, void* dv, void* workspace,
+               size_t workspace_bytes, int B, int H, int H_kv, int N, int d, float scale,
+               int causal, int dtype, void* stream);
+
+/*
  * fa_bwd without a caller-supplied workspace, for callers that cannot allocate
  * device memory when they run the backward -- for example a plug-in called
  * from a host framework that owns the device memory budget and forbids

@@ -20,6 +20,10 @@ Functions (numpy in, numpy out; every array is promoted to float64):
   ("FlashAttention-1" page, 10.2.4): dV = P^T dO, dP = dO V^T,
   dS = P o (dP - delta), delta_i = dO_i . O_i, dQ = scale dS K,
   dK = scale dS^T Q.
+* ``attn_fwd_gqa`` / ``attn_bwd_gqa`` -- grouped-query attention ("5.4
+  FlashAttention" page, GQA heading): each K/V head repeated for its group of
+  query heads; dK, dV summed over the group (chain rule through the shared
+  operand).
 * ``e4m3_decode(codes, descale)`` / ``e4m3_encode(x)`` -- OCP FP8 E4M3.
 
 Tensors are ``[..., N, d]``; leading dimensions are flattened into heads.
@@ -136,6 +140,36 @@ def attn_bwd(q, k, v, do, scale, causal=False, nthreads=0):
     lib().oracle_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(do), BH, N, d, float(scale),
                      int(bool(causal)), _ptr(dq), _ptr(dk), _ptr(dv), int(nthreads))
     return dq, dk, dv
+
+
+def _group(q, k, v):
+    """[B, H, N, d] queries against [B, H_kv, N, d] keys/values: the group size."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    if q.ndim != 4 or k.shape != v.shape or k.ndim != 4 or q.shape[0] != k.shape[0] \
+            or q.shape[2:] != k.shape[2:] or k.shape[1] < 1 or q.shape[1] % k.shape[1]:
+        raise ValueError("grouped-query: q [B, H, N, d], k and v [B, H_kv, N, d], H_kv | H")
+    return q, k, v, q.shape[1] // k.shape[1]
+
+
+def attn_fwd_gqa(q, k, v, scale, causal=False, nthreads=0):
+    """Grouped-query forward ("5.4 FlashAttention" page, the GQA heading): query
+    head h reads K/V head h // (H / H_kv).  Each K/V head is repeated for its group
+    and the plain forward runs per query head."""
+    q, k, v, g = _group(q, k, v)
+    return attn_fwd(q, np.repeat(k, g, axis=1), np.repeat(v, g, axis=1), scale, causal, nthreads)
+
+
+def attn_bwd_gqa(q, k, v, do, scale, causal=False, nthreads=0):
+    """Gradients of L = <dO, O> for grouped-query attention.  K/V head j enters
+    the forward of every query head of its group, so by the chain rule its dK, dV
+    are the sums of the per-query-head gradients ("FlashAttention-1" page, 10.2.4,
+    per head) over the group; dQ is per query head."""
+    q, k, v, g = _group(q, k, v)
+    dq, dk, dv = attn_bwd(q, np.repeat(k, g, axis=1), np.repeat(v, g, axis=1), do, scale, causal,
+                          nthreads)
+    B, H_kv, N, d = k.shape
+    return (dq, dk.reshape(B, H_kv, g, N, d).sum(axis=2),
+            dv.reshape(B, H_kv, g, N, d).sum(axis=2))
 
 
 def e4m3_decode(codes, descale=1.0):

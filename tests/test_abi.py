@@ -110,3 +110,15 @@ def test_bwd_argument_errors(L):
     assert b(dtype=9) == 1
     assert b(dtype=0) == 2
     assert b(d=96) == 2
+
+
+def test_bwd_gqa_argument_errors(L):
+    ws = fa.fa_bwd_workspace_size(1, 4, 128, 64)
+
+    def b(H=4, H_kv=2, d=64, ws_bytes=ws):
+        return L.fa_bwd_gqa(P, P, P, P, P, P, P, P, P, P, ws_bytes, 1, H, H_kv, 128, d, 0.125, 0,
+                            1, None)
+    assert b(H_kv=0) == 1
+    assert b(H_kv=3) == 1                # 4 % 3 != 0
+    assert b(ws_bytes=ws - 4) == 1
+    assert b(d=96) == 2

@@ -371,3 +371,41 @@ def test_e4m3_encode_matches_torch_rne():
     # every finite code round-trips
     codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
     np.testing.assert_array_equal(oracle.e4m3_encode(oracle.e4m3_decode(codes)), codes)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_gqa_bwd_matches_finite_differences_of_shared_kv(causal):
+    # grouped-query: 4 query heads share 2 K/V heads.  Perturbing one element of a
+    # shared K or V head moves every query head of its group, so the finite
+    # difference of L = <dO, O> checks the group sum (a gradient taken from one
+    # query head only, or summed over the wrong group, fails here).
+    B, H, H_kv, N, d, scale, h = 1, 4, 2, 5, 3, 0.8, 1e-6
+    q, do = rnd(60, B, H, N, d), rnd(61, B, H, N, d)
+    k, v = rnd(62, B, H_kv, N, d), rnd(63, B, H_kv, N, d)
+    dq, dk, dv = oracle.attn_bwd_gqa(q, k, v, do, scale, causal)
+    assert dk.shape == k.shape and dv.shape == v.shape and dq.shape == q.shape
+
+    def L(qq, kk, vv):
+        o, _ = oracle.attn_fwd(qq, np.repeat(kk, 2, axis=1), np.repeat(vv, 2, axis=1), scale,
+                               causal)
+        return float(np.sum(o * do))
+
+    for which, got in enumerate((dq, dk, dv)):
+        for idx in [(0, 0, 0, 0), (0, 1, 4, 2), (0, 1, 2, 1)] + ([(0, 3, 3, 0)] if which == 0 else []):
+            xs_p = [q.copy(), k.copy(), v.copy()]
+            xs_m = [q.copy(), k.copy(), v.copy()]
+            xs_p[which][idx] += h
+            xs_m[which][idx] -= h
+            fd = (L(*xs_p) - L(*xs_m)) / (2 * h)
+            assert abs(fd - got[idx]) <= 1e-7 * max(1.0, abs(fd))
+
+
+def test_gqa_with_one_group_per_head_is_plain_attention():
+    # H_kv = H: the grouped entry points reduce to the plain ones
+    q, k, v, do = (rnd(70 + i, 2, 3, 6, 4) for i in range(4))
+    a = oracle.attn_bwd_gqa(q, k, v, do, 0.5, True)
+    b = oracle.attn_bwd(q, k, v, do, 0.5, True)
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
+    with pytest.raises(ValueError):
+        oracle.attn_fwd_gqa(q, k[:, :2], v[:, :2], 0.5)
