@@ -24,6 +24,10 @@ Functions (numpy in, numpy out; every array is promoted to float64):
   FlashAttention" page, GQA heading): each K/V head repeated for its group of
   query heads; dK, dV summed over the group (chain rule through the shared
   operand).
+* ``attn_fwd_kv_shard(q, k, v, scale, causal, q_offset, kv_offset)`` -- the
+  forward restricted to one shard of keys (numpy), rows with no key: O = 0,
+  lse = -inf; ``lse_merge(o_parts, lse_parts)`` -- the two-state combination
+  of "FlashAttention-1" 10.2.2 applied to normalised partial outputs.
 * ``e4m3_decode(codes, descale)`` / ``e4m3_encode(x)`` -- OCP FP8 E4M3.
 
 Tensors are ``[..., N, d]``; leading dimensions are flattened into heads.
@@ -170,6 +174,50 @@ def attn_bwd_gqa(q, k, v, do, scale, causal=False, nthreads=0):
     B, H_kv, N, d = k.shape
     return (dq, dk.reshape(B, H_kv, g, N, d).sum(axis=2),
             dv.reshape(B, H_kv, g, N, d).sum(axis=2))
+
+
+def attn_fwd_kv_shard(q, k, v, scale, causal=False, q_offset=0, kv_offset=0):
+    """Attention of queries at global positions q_offset + i against one shard of
+    keys at global positions kv_offset + j ([..., N_q, d] against [..., N_kv, d]).
+
+    Standard attention written out ("FlashAttention-1" page, 10.2.1) on the keys
+    the shard holds: S = scale Q K^T, causal mask kv_offset + j > q_offset + i,
+    stable softmax, O = P V, lse = m + ln l.  A row that sees no key of the shard
+    has l = 0: it returns O = 0 and lse = -inf, so that it drops out of the merge.
+    Returns (O [..., N_q, d], lse [..., N_q])."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    if k.shape != v.shape or q.shape[:-2] != k.shape[:-2] or q.shape[-1] != k.shape[-1]:
+        raise ValueError("q [..., N_q, d]; k and v [..., N_kv, d] with the same leading dims")
+    S = scale * np.matmul(q, np.swapaxes(k, -1, -2))
+    Nq, Nkv = q.shape[-2], k.shape[-2]
+    if causal:
+        masked = (kv_offset + np.arange(Nkv))[None, :] > (q_offset + np.arange(Nq))[:, None]
+        S = np.where(masked, -np.inf, S)
+    m = S.max(axis=-1, initial=-np.inf)
+    seen = np.isfinite(m)
+    P = np.exp(S - np.where(seen, m, 0.0)[..., None])
+    l = P.sum(axis=-1)
+    o = np.matmul(P, v) / np.where(seen, l, 1.0)[..., None]
+    lse = np.where(seen, m + np.log(np.where(seen, l, 1.0)), -np.inf)
+    return o, lse
+
+
+def lse_merge(o_parts, lse_parts):
+    """Merge attention outputs computed over disjoint key sets ("FlashAttention-1"
+    page, 10.2.2: two partial softmax states combine through their maxima and
+    sums).  With each part normalised, part s carries l_s = exp(lse_s) of the
+    total, so lse = ln sum_s exp(lse_s) and O = sum_s exp(lse_s - lse) O_s.
+    o_parts [S, ..., d], lse_parts [S, ...].  Parts with lse = -inf contribute
+    nothing; if every part is -inf the row is O = 0, lse = -inf."""
+    o, L = _f64(o_parts), _f64(lse_parts)
+    m = L.max(axis=0)
+    seen = np.isfinite(m)
+    mm = np.where(seen, m, 0.0)
+    w = np.exp(L - mm[None])
+    tot = w.sum(axis=0)
+    lse = np.where(seen, mm + np.log(np.where(seen, tot, 1.0)), -np.inf)
+    out = (w[..., None] * o).sum(axis=0) / np.where(seen, tot, 1.0)[..., None]
+    return out, lse
 
 
 def e4m3_decode(codes, descale=1.0):

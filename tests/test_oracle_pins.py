@@ -409,3 +409,85 @@ def test_gqa_with_one_group_per_head_is_plain_attention():
         np.testing.assert_array_equal(x, y)
     with pytest.raises(ValueError):
         oracle.attn_fwd_gqa(q, k[:, :2], v[:, :2], 0.5)
+
+
+# ---- key shards and the lse merge ("FlashAttention-1" 10.2.2 combination rule)
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_kv_shard_whole_sequence_is_the_forward(causal):
+    # one shard holding every key is plain attention: the numpy shard oracle
+    # against the C oracle (two independent codings of 10.2.1)
+    q, k, v = rnd(80, 2, 9, 5), rnd(81, 2, 9, 5), rnd(82, 2, 9, 5)
+    o1, l1 = oracle.attn_fwd_kv_shard(q, k, v, 0.7, causal)
+    o2, l2 = oracle.attn_fwd(q, k, v, 0.7, causal)
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("cuts", [(4,), (1, 7), (3, 5, 6), (0, 2, 11)])
+def test_merging_key_shards_gives_the_full_forward(causal, cuts):
+    # split the keys at `cuts`, attend each shard with its global offset, merge:
+    # the full forward of the C oracle.  A wrong merge weight, a dropped shard or a
+    # causal offset of the wrong sign fails here.
+    N, d = 12, 4
+    q, k, v = rnd(83, 1, 2, N, d), rnd(84, 1, 2, N, d), rnd(85, 1, 2, N, d)
+    edges = [0, *cuts, N]
+    parts = [oracle.attn_fwd_kv_shard(q, k[..., a:b, :], v[..., a:b, :], 0.9, causal,
+                                      q_offset=0, kv_offset=a)
+             for a, b in zip(edges[:-1], edges[1:])]
+    o, lse = oracle.lse_merge(np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]))
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, 0.9, causal)
+    np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse, lse_ref, rtol=0, atol=1e-13)
+
+
+def test_query_shards_with_offsets_tile_the_causal_forward():
+    # queries split as well: block (qa..qb) x (ka..kb) with both offsets, merged
+    # over the key shards, equals the rows qa..qb of the full causal forward
+    N, d = 10, 3
+    q, k, v = rnd(86, N, d), rnd(87, N, d), rnd(88, N, d)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, 1.1, True)
+    edges = [0, 3, 8, 10]
+    for qa, qb in zip(edges[:-1], edges[1:]):
+        parts = [oracle.attn_fwd_kv_shard(q[qa:qb], k[ka:kb], v[ka:kb], 1.1, True, qa, ka)
+                 for ka, kb in zip(edges[:-1], edges[1:])]
+        o, lse = oracle.lse_merge(np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]))
+        np.testing.assert_allclose(o, o_ref[qa:qb], rtol=0, atol=1e-13)
+        np.testing.assert_allclose(lse, lse_ref[qa:qb], rtol=0, atol=1e-13)
+
+
+def test_kv_shard_rows_that_see_no_key():
+    # keys 5.. against queries 0..3 under the causal mask: nothing visible
+    q, k, v = rnd(89, 4, 3), rnd(90, 2, 3), rnd(91, 2, 3)
+    o, lse = oracle.attn_fwd_kv_shard(q, k, v, 1.0, True, q_offset=0, kv_offset=5)
+    assert np.all(o == 0) and np.all(lse == -np.inf)
+    # query 5 sees exactly key 5: O = V_0 of the shard, lse = scale q.k
+    o, lse = oracle.attn_fwd_kv_shard(q, k, v, 1.0, True, q_offset=2, kv_offset=5)
+    assert np.all(o[:3] == 0) and np.all(lse[:3] == -np.inf)
+    np.testing.assert_allclose(o[3], v[0], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(lse[3], q[3] @ k[0], rtol=0, atol=1e-14)
+
+
+def test_lse_merge_closed_forms():
+    o_a, o_b = rnd(92, 5, 4), rnd(93, 5, 4)
+    # two parts of equal weight: the mean, and lse + ln 2
+    o, lse = oracle.lse_merge(np.stack([o_a, o_b]), np.full((2, 5), 1.5))
+    np.testing.assert_allclose(o, (o_a + o_b) / 2, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(lse, 1.5 + math.log(2), rtol=0, atol=1e-15)
+    # weights e^1 : e^3 -> O = (o_a + e^2 o_b) / (1 + e^2), lse = ln(e + e^3)
+    o, lse = oracle.lse_merge(np.stack([o_a, o_b]), np.stack([np.full(5, 1.0), np.full(5, 3.0)]))
+    w = math.exp(2.0)
+    np.testing.assert_allclose(o, (o_a + w * o_b) / (1 + w), rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lse, math.log(math.e + math.e ** 3), rtol=0, atol=1e-14)
+    # a -inf part drops out whatever its O holds; all -inf gives O = 0, lse = -inf
+    lse_in = np.stack([np.full(5, -np.inf), np.full(5, 0.25)])
+    o, lse = oracle.lse_merge(np.stack([o_a, o_b]), lse_in)
+    np.testing.assert_array_equal(o, o_b)
+    np.testing.assert_array_equal(lse, np.full(5, 0.25))
+    o, lse = oracle.lse_merge(np.stack([o_a, o_b]), np.full((2, 5), -np.inf))
+    assert np.all(o == 0) and np.all(lse == -np.inf)
+    # very different magnitudes stay finite (the merge subtracts the max)
+    o, lse = oracle.lse_merge(np.stack([o_a, o_b]), np.stack([np.full(5, 800.0), np.full(5, -800.0)]))
+    np.testing.assert_allclose(o, o_a, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(lse, 800.0, rtol=0, atol=1e-12)
