@@ -15,6 +15,12 @@ launch stream, inputs resident in HBM); ``parts`` gives each stage alone.
 ``e2e`` times the same step through the public API with pinned host buffers:
 inputs copied in and outputs copied out inside the timed region.
 
+``extras`` times the variant rows alone, after the step and outside ``value``
+(10 launches each after 3 warm-ups): backward at d=128 and causal, FP8 causal
+and per-head, grouped-query forward/backward (32 query heads on 8 K/V heads),
+and the forward sharded over 4 key blocks of the sequence plus the lse merge
+(with the merge kernel's achieved HBM bandwidth).
+
 ``--impl reference`` times the fp64 CPU oracle instead (the comparison arm) on a
 bounded sample of the same workload, on this machine's host cores.
 
@@ -208,6 +214,113 @@ def run_part_e2e(fa, P, stream):
         P["host_out"][n].copy_(t, non_blocking=True)
 
 
+# ---------------------------------------------------------------- extras
+# The widened rows, each timed alone after the main step (not part of `value`):
+# name, what, B, H, H_kv, N, d, causal
+EXTRAS = [
+    ("bwd_bf16_b1h32n16384d128", "bwd", 1, 32, 32, 16384, 128, False),
+    ("bwd_bf16_b1h32n16384d128_causal", "bwd", 1, 32, 32, 16384, 128, True),
+    ("bwd_bf16_b4h16n2048d64_causal", "bwd", 4, 16, 16, 2048, 64, True),
+    ("fwd_e4m3_b4h16n4096d128_causal", "fwd8", 4, 16, 16, 4096, 128, True),
+    ("fwd_e4m3_per_head_b4h16n4096d128", "fwd8h", 4, 16, 16, 4096, 128, False),
+    ("fwd_gqa_bf16_b1h32hkv8n16384d128_causal", "gqa_fwd", 1, 32, 8, 16384, 128, True),
+    ("bwd_gqa_bf16_b1h32hkv8n16384d128_causal", "gqa_bwd", 1, 32, 8, 16384, 128, True),
+    ("fwd_seq4shards_bf16_b1h32n16384d128_causal", "shard4", 1, 32, 32, 16384, 128, True),
+]
+
+
+def make_extra(torch, fa, inputs, ex, dev, stream):
+    """Inputs on the device and a closure that runs the row once on `stream`.
+    Returns (run, flop, sub) where sub names event-split pieces (or None)."""
+    name, what, B, H, H_kv, N, d, causal = ex
+    s = 1.0 / math.sqrt(d)
+    bf = lambda shape, seed: inputs.cast(inputs.normal(shape, seed), "bf16").to(dev)
+    f_fwd = flops("fwd", B, H, N, d, causal)
+    f_bwd = flops("fwdbwd", B, H, N, d, causal) - f_fwd
+    if what in ("fwd8", "fwd8h"):
+        x = inputs.attention_inputs(B, H, N, d, "e4m3")
+        q8, k8, v8 = x["q"].to(dev), x["k"].to(dev), x["v"].to(dev)
+        o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        if what == "fwd8":
+            ds = (x["q_descale"], x["k_descale"], x["v_descale"])
+            return (lambda: fa.fa_fwd_fp8(q8, k8, v8, o, lse, *ds, s, causal, stream)), f_fwd, None
+        hd = [torch.full((B * H,), float(x[n + "_descale"]), device=dev) for n in "qkv"]
+        return (lambda: fa.fa_fwd_fp8_per_head(q8, k8, v8, o, lse, *hd, s, causal, stream)), f_fwd, None
+    q, do = bf((B, H, N, d), 42), bf((B, H, N, d), 45)
+    k, v = bf((B, H_kv, N, d), 43), bf((B, H_kv, N, d), 44)
+    o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    if what == "gqa_fwd":
+        return (lambda: fa.fa_fwd_gqa(q, k, v, o, lse, s, causal, fa.FA_BF16, stream)), f_fwd, None
+    if what in ("bwd", "gqa_bwd"):
+        (fa.fa_fwd if H == H_kv else fa.fa_fwd_gqa)(q, k, v, o, lse, s, causal, fa.FA_BF16, stream)
+        ws = torch.empty(fa.fa_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        fn = fa.fa_bwd if H == H_kv else fa.fa_bwd_gqa
+        return (lambda: fn(q, k, v, o, lse, do, dq, dk, dv, ws, s, causal, fa.FA_BF16, stream)), \
+            f_bwd, None
+    # sequence sharded: every query against 4 key shards, then the lse merge
+    S = 4
+    n = N // S
+    ks = [k[:, :, t * n:(t + 1) * n].contiguous() for t in range(S)]
+    vs = [v[:, :, t * n:(t + 1) * n].contiguous() for t in range(S)]
+    o_p = torch.empty((S, B, H, N, d), dtype=torch.float32, device=dev)
+    l_p = torch.empty((S, B, H, N), dtype=torch.float32, device=dev)
+    mid = torch.cuda.Event(enable_timing=True)
+
+    def run():
+        for t in range(S):
+            fa.fa_fwd_kv_shard(q, ks[t], vs[t], o_p[t], l_p[t], s, causal, 0, t * n,
+                               fa.FA_BF16, stream)
+        mid.record(stream)
+        fa.fa_lse_merge(o_p, l_p, o, lse, fa.FA_BF16, stream)
+    rows = B * H * N
+    merge_bytes = S * rows * (4 * d + 4) + rows * (2 * d + 4)
+    return run, f_fwd, {"mid": mid, "merge_bytes": merge_bytes, "launches": S + 1}
+
+
+def time_extras(torch, fa, inputs, dev, stream, pk, iters=10, warmup=3):
+    out = {}
+    for ex in EXTRAS:
+        name, what = ex[0], ex[1]
+        run, fl, sub = make_extra(torch, fa, inputs, ex, dev, stream)
+        for _ in range(warmup):
+            run()
+        torch.cuda.synchronize()
+        ms, merge_ms = [], []
+        for _ in range(iters):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            run()
+            e1.record(stream)
+            e1.synchronize()
+            ms.append(e0.elapsed_time(e1))
+            if sub is not None:
+                merge_ms.append(sub["mid"].elapsed_time(e1))
+        st = fa.fa_last_device_error()
+        if st != 0:
+            raise RuntimeError(f"{name}: device status {fa.fa_status_string(st)}")
+        mean = sum(ms) / len(ms)
+        tf = fl / (mean * 1e-3) / 1e12
+        rec = {"ms": round(mean, 4), "tflops": round(tf, 1), "flop": fl}
+        if what.startswith("fwd8"):
+            rec["dtype"] = "e4m3"
+        else:
+            rec["pct_of_peak"] = round(100 * tf / pk["bf16"], 1)
+        if sub is not None:
+            mm = sum(merge_ms) / len(merge_ms)
+            gbs = sub["merge_bytes"] / (mm * 1e-3) / 1e9
+            rec["merge"] = {"kernel": "lse_merge_kernel<128,bf16>", "bound": "hbm", "ms": round(mm, 4),
+                            "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                            "frac": round(gbs / pk["hbm_gbs"], 4),
+                            "algorithmic_bytes": sub["merge_bytes"]}
+        out[name] = rec
+        del run, sub
+        torch.cuda.empty_cache()
+    return out
+
+
 def fp8_peak(torch, dev):
     """Dense e4m3 GEMM throughput (torch._scaled_mm, 8192^3, best of 10)."""
     try:
@@ -355,6 +468,11 @@ def bench_ours(args):
     value = job_tflops(world, step_flop, ms_step)
     pk = peaks()
     fp8_tf, fp8_how = fp8_peak(torch, dev)
+    extras = None if args.no_extras else time_extras(torch, fa, inputs, dev, stream, pk)
+    if extras:
+        for rec in extras.values():
+            if rec.get("dtype") == "e4m3" and fp8_tf:
+                rec["pct_of_fp8_peak"] = round(100 * rec["tflops"] / fp8_tf, 1)
 
     part_out = {}
     for P, ms in zip(parts, part_ms):
@@ -392,6 +510,7 @@ def bench_ours(args):
                    "l2": "inputs larger than L2: each part follows a part that streams >129 MB"},
         "pct_of_peak": round(100 * value / world / pk["bf16"], 1),
         "parts": part_out,
+        "extras": extras,
         "fp8_peak_tflops": None if fp8_tf is None else round(fp8_tf, 1), "fp8_peak_how": fp8_how,
         "roofline": roofline,
         "e2e": {"value": round(job_tflops(world, step_flop, e2e_ms), 1), "unit": UNIT,
@@ -451,6 +570,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the separately timed variant rows (``extras``)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

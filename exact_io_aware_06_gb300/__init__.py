@@ -52,6 +52,11 @@ def lib():
         L.fa_fwd_gqa.restype = i
         L.fa_fwd_fp8_per_head.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
         L.fa_fwd_fp8_per_head.restype = i
+        ll = ctypes.c_longlong
+        L.fa_fwd_kv_shard.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, ll, ll, i, vp]
+        L.fa_fwd_kv_shard.restype = i
+        L.fa_lse_merge.argtypes = [vp, vp, i, vp, vp, i, i, i, i, i, vp]
+        L.fa_lse_merge.restype = i
         L.fa_bwd_workspace_size.argtypes = [i, i, i, i]
         L.fa_bwd_workspace_size.restype = sz
         L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, f, i, i, vp]
@@ -139,6 +144,28 @@ def fa_fwd_fp8_per_head(q8, k8, v8, o, lse, q_descale, k_descale, v_descale, sca
                                      _ptr(q_descale), _ptr(k_descale), _ptr(v_descale), B, H, N,
                                      d, float(scale), int(bool(causal)), _stream(stream)),
            "fa_fwd_fp8_per_head")
+
+
+def fa_fwd_kv_shard(q, k, v, o_part, lse_part, scale, causal, q_offset, kv_offset,
+                    dtype=FA_BF16, stream=None):
+    """Forward of q [B, H, N_q, d] over one key shard k, v [B, H_kv, N_kv, d] at the
+    given global offsets; o_part float32 [B, H, N_q, d], lse_part [B, H, N_q]."""
+    B, H, N_q, d = _shape(q)
+    H_kv, N_kv = _shape(k)[1], _shape(k)[2]
+    _check(lib().fa_fwd_kv_shard(_ptr(q), _ptr(k), _ptr(v), _ptr(o_part), _ptr(lse_part), B, H,
+                                 H_kv, N_q, N_kv, d, float(scale), int(bool(causal)),
+                                 int(q_offset), int(kv_offset), int(dtype), _stream(stream)),
+           "fa_fwd_kv_shard")
+
+
+def fa_lse_merge(o_parts, lse_parts, o, lse, dtype, stream=None):
+    """Merge stacked shard outputs o_parts [S, B, H, N, d] (float32), lse_parts
+    [S, B, H, N] into o [B, H, N, d] (bf16 or float32 per dtype) and lse (or None)."""
+    S, B, H, N, d = (int(x) for x in o_parts.shape)
+    if tuple(lse_parts.shape) != (S, B, H, N) or tuple(o.shape) != (B, H, N, d):
+        raise ValueError("fa_lse_merge: shapes do not match")
+    _check(lib().fa_lse_merge(_ptr(o_parts), _ptr(lse_parts), S, _ptr(o), _ptr(lse), B, H, N, d,
+                              int(dtype), _stream(stream)), "fa_lse_merge")
 
 
 def fa_bwd_workspace_size(B, H, N, d):

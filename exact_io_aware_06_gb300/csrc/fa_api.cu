@@ -180,6 +180,50 @@ __attribute__((visibility("default"))) int fa_fwd_fp8_per_head(
                                       static_cast<cudaStream_t>(stream)));
 }
 
+__attribute__((visibility("default"))) int fa_fwd_kv_shard(
+    const void* q, const void* k, const void* v, float* o_part, float* lse_part, int B, int H,
+    int H_kv, int N_q, int N_kv, int d, float scale, int causal, long long q_offset,
+    long long kv_offset, int dtype, void* stream) {
+    int rc = check_common(q, k, v, o_part, lse_part, B, H, N_q);
+    if (rc != FA_OK) return rc;
+    if (lse_part == nullptr || N_kv < 1) return FA_ERR_INVALID_ARG;
+    if (N_kv > (1 << 24)) return FA_ERR_UNSUPPORTED;
+    if (!std::isfinite(scale) || H_kv < 1 || H % H_kv != 0) return FA_ERR_INVALID_ARG;
+    if (dtype != FA_F32 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
+    if (dtype != FA_BF16 || (d != 64 && d != 128)) return FA_ERR_UNSUPPORTED;
+    // key j reaches query i iff kv_offset + j <= q_offset + i; beyond these bounds the
+    // offset difference no longer changes which keys a row sees
+    long long delta = q_offset - kv_offset;
+    if (delta > N_kv) delta = N_kv;
+    if (delta < -static_cast<long long>(N_q) - 1) delta = -static_cast<long long>(N_q) - 1;
+    int err = FA_OK;
+    int* st = status_word(&err);
+    if (st == nullptr) return err;
+    DevCtl ctl{st, g_wait_ns.load()};
+    const float c_log2 = scale * 1.4426950408889634f;
+    return from_cuda(launch_fwd_kv_shard(q, k, v, o_part, lse_part, B, H, H_kv, N_q, N_kv, d,
+                                         c_log2, causal ? 1 : 0, static_cast<int>(delta), ctl,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+__attribute__((visibility("default"))) int fa_lse_merge(const float* o_parts,
+                                                        const float* lse_parts, int n_parts,
+                                                        void* o, float* lse, int B, int H, int N,
+                                                        int d, int dtype, void* stream) {
+    if (o_parts == nullptr || lse_parts == nullptr || o == nullptr) return FA_ERR_INVALID_ARG;
+    if (!aligned16(o_parts) || !aligned16(lse_parts) || !aligned16(o)) return FA_ERR_INVALID_ARG;
+    if (lse != nullptr && !aligned16(lse)) return FA_ERR_INVALID_ARG;
+    if (n_parts < 1 || B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+    if (dtype != FA_F32 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    const size_t rows = static_cast<size_t>(B) * H * N;
+    if (rows * static_cast<size_t>(n_parts) > (static_cast<size_t>(1) << 40))
+        return FA_ERR_UNSUPPORTED;
+    return from_cuda(static_cast<int>(launch_lse_merge(o_parts, lse_parts, n_parts, rows, d, o,
+                                                       dtype == FA_F32 ? 1 : 0, lse,
+                                                       static_cast<cudaStream_t>(stream))));
+}
+
 __attribute__((visibility("default"))) size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
     if (B < 1 || H < 1 || N < 1 || d < 1) return 0;
     return bwd_workspace_bytes(B * H, N, d);

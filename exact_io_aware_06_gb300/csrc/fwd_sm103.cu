@@ -46,9 +46,11 @@ constexpr int kThreads = 384;    // 12 warps
 constexpr float kTau = 8.0f;     // lazy-rescale threshold, log2 units
 
 struct FwdArgs {
-    void* o;
+    void* o;          // bf16 [BH][N][D], or float32 when o_f32
     float* lse;
-    int N;
+    int N;            // query rows per head
+    int N_kv;         // keys per head (= N except for a key shard)
+    int delta;        // causal: key j reaches query i iff j <= i + delta (0 unless sharded)
     int n_pairs;      // query-tile pairs per head
     float c_log2;     // scale * log2(e) (times the FP8 descales)
     float o_scale;    // multiplies O at the end (FP8: v descale), 1 otherwise
@@ -163,7 +165,9 @@ __device__ __forceinline__ float block_extreme(const uint32_t (&r)[128], bool wa
     return min3f(a[0], a[1], fminf(a[2], a[3]));
 }
 
-template <int D, bool FP8>
+// SHARD: forward over a key shard (N_kv keys, causal offset delta, float32 O,
+// rows that see no key); compiled separately so the plain forward carries none of it.
+template <int D, bool FP8, bool SHARD>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const FwdArgs args) {
@@ -184,8 +188,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int pair = args.n_pairs - 1 - (blockIdx.x % args.n_pairs);
     const int r0 = pair * 2 * kBM;
     const int N = args.N;
-    const int kv_end = args.causal ? min(N, r0 + 2 * kBM) : N;
-    const int n_kv = (kv_end + kBN - 1) / kBN;
+    const int N_kv = SHARD ? args.N_kv : N;
+    const int delta = SHARD ? args.delta : 0;
+    // keys this pair of tiles can see; none at all when a causal key shard lies
+    // wholly after these queries
+    const int kv_end = args.causal ? min(N_kv, r0 + 2 * kBM + delta) : N_kv;
+    const int n_kv = (!SHARD || kv_end > 0) ? (kv_end + kBN - 1) / kBN : 0;
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
@@ -299,6 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mma_bf16_ts(tmem + colO, tmem + colP + kk * 8, db, C::kIdescO, acc || kk > 0);
                 }
             };
+            if (SHARD && n_kv == 0) ok = false;  // nothing to multiply; not an error
             if (ok) ok = mbar_wait(smem_u32(&bars.k_full[0]), 0, lim, &abort_flag);
             if (ok) {
                 tc_fence_after();
@@ -341,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_commit(smem_u32(&bars.o_done[1]));
                 }
             }
-            if (!ok) record_timeout(args.ctl, &abort_flag);
+            if (!ok && (!SHARD || n_kv > 0)) record_timeout(args.ctl, &abort_flag);
             // drain every MMA this thread issued before TMEM is released
             mma_commit(smem_u32(&bars.drain));
             const volatile int never = 0;
@@ -384,9 +393,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_ld_fence(r);
 
             const int kv0 = j * kBN;
-            if ((kv0 + kBN > N) || (args.causal && kv0 + kBN - 1 > qrow)) {
-                // keys >= N, and keys after this query row when causal, drop out
-                const int valid = min(N - kv0, args.causal ? qrow - kv0 + 1 : kBN);
+            const int qlast = qrow + delta;  // last key this row reaches when causal
+            if ((kv0 + kBN > N_kv) || (args.causal && kv0 + kBN - 1 > qlast)) {
+                // keys >= N_kv, and keys after this query row when causal, drop out
+                const int valid = min(N_kv - kv0, args.causal ? qlast - kv0 + 1 : kBN);
 #pragma unroll
                 for (int i = 0; i < 128; ++i)
                     if (i >= valid) r[i] = mask_bits;
@@ -456,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive(smem_u32(&bars.p_full[t]));
         }
-        if (ok) {
+        if (ok && (!SHARD || n_kv > 0)) {
             ok = mbar_wait(smem_u32(&bars.o_done[t]), 0, lim, &abort_flag);
             ok = __all_sync(0xffffffffu, ok);
         }
@@ -464,13 +474,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) record_timeout(args.ctl, &abort_flag);
         } else {
             tc_fence_after();
-            const float inv = o_scale / l;
+            // a row that saw no key (l = 0; only in a causal key shard) gives O = 0 and
+            // lse = -inf: its O columns hold P V with P = 0, or were never written
+            const float inv = (!SHARD || l > 0.f) ? o_scale / l : 0.f;
             const size_t orow = (static_cast<size_t>(bh) * N + qrow) * D;
 #pragma unroll
             for (int q4 = 0; q4 < D / 32; ++q4) {
                 uint32_t ov[32];
-                tmem_ld32(lane_base + colO + 32 * q4, ov);
-                if (qrow < N) {
+                if (!SHARD || n_kv > 0) {
+                    tmem_ld32(lane_base + colO + 32 * q4, ov);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) ov[i] = 0u;
+                }
+                if (SHARD && qrow < N) {
+                    float4* out = reinterpret_cast<float4*>(static_cast<float*>(args.o) + orow + 32 * q4);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        out[i] = make_float4(__uint_as_float(ov[4 * i]) * inv, __uint_as_float(ov[4 * i + 1]) * inv,
+                                             __uint_as_float(ov[4 * i + 2]) * inv, __uint_as_float(ov[4 * i + 3]) * inv);
+                } else if (qrow < N) {
                     uint32_t w[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
@@ -495,24 +518,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D, bool FP8>
+template <int D, bool FP8, bool SHARD>
 int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-                int H_kv, int N, float c_log2, float o_scale, const float* qd, const float* kd,
-                const float* vd, int causal, DevCtl ctl, cudaStream_t s) {
+                int H_kv, int N, int N_kv, int delta, float c_log2, float o_scale,
+                const float* qd, const float* kd, const float* vd, int causal, DevCtl ctl,
+                cudaStream_t s) {
     const int BH = B * H, BH_kv = B * H_kv;
     using C = Cfg<D, FP8>;
     const CUtensorMapDataType dt =
         FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     CUtensorMap tq, tk, tv;
     int rc = make_map_3d(&tq, q, dt, C::kElem, D, N, BH, C::kBoxX, kBM);
-    if (rc == 0) rc = make_map_3d(&tk, k, dt, C::kElem, D, N, BH_kv, C::kBoxX, kBN);
-    if (rc == 0) rc = make_map_3d(&tv, v, dt, C::kElem, D, N, BH_kv, C::kBoxX, kBN);
+    if (rc == 0) rc = make_map_3d(&tk, k, dt, C::kElem, D, N_kv, BH_kv, C::kBoxX, kBN);
+    if (rc == 0) rc = make_map_3d(&tv, v, dt, C::kElem, D, N_kv, BH_kv, C::kBoxX, kBN);
     if (rc != 0) return rc;
     static uint64_t attr_set = 0;  // per template instance, one bit per device
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 64 || !(attr_set & (1ull << dev))) {
-        cudaError_t e = cudaFuncSetAttribute(fwd_sm103_kernel<D, FP8>,
+        cudaError_t e = cudaFuncSetAttribute(fwd_sm103_kernel<D, FP8, SHARD>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::kSmemAlloc);
         if (e != cudaSuccess) return static_cast<int>(e);
@@ -522,6 +546,8 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse
     a.o = o;
     a.lse = lse;
     a.N = N;
+    a.N_kv = N_kv;
+    a.delta = delta;
     a.n_pairs = (N + 2 * kBM - 1) / (2 * kBM);
     a.c_log2 = c_log2;
     a.o_scale = o_scale;
@@ -533,7 +559,7 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse
     a.v_descale = vd;
     a.ctl = ctl;
     dim3 grid(a.n_pairs * BH);
-    fwd_sm103_kernel<D, FP8><<<grid, kThreads, C::kSmemAlloc, s>>>(tq, tk, tv, a);
+    fwd_sm103_kernel<D, FP8, SHARD><<<grid, kThreads, C::kSmemAlloc, s>>>(tq, tk, tv, a);
     return static_cast<int>(cudaGetLastError());
 }
 
@@ -544,13 +570,23 @@ int launch_fwd_sm103(const void* q, const void* k, const void* v, void* o, float
                      const float* kd, const float* vd, int causal, bool is_fp8, DevCtl ctl,
                      cudaStream_t s) {
     if (is_fp8)
-        return launch_impl<128, true>(q, k, v, o, lse, B, H, H_kv, N, c_log2, o_scale, qd, kd, vd,
-                                      causal, ctl, s);
+        return launch_impl<128, true, false>(q, k, v, o, lse, B, H, H_kv, N, N, 0, c_log2,
+                                             o_scale, qd, kd, vd, causal, ctl, s);
     if (d == 64)
-        return launch_impl<64, false>(q, k, v, o, lse, B, H, H_kv, N, c_log2, o_scale, qd, kd, vd,
-                                      causal, ctl, s);
-    return launch_impl<128, false>(q, k, v, o, lse, B, H, H_kv, N, c_log2, o_scale, qd, kd, vd,
-                                   causal, ctl, s);
+        return launch_impl<64, false, false>(q, k, v, o, lse, B, H, H_kv, N, N, 0, c_log2,
+                                             o_scale, qd, kd, vd, causal, ctl, s);
+    return launch_impl<128, false, false>(q, k, v, o, lse, B, H, H_kv, N, N, 0, c_log2, o_scale,
+                                          qd, kd, vd, causal, ctl, s);
+}
+
+int launch_fwd_kv_shard(const void* q, const void* k, const void* v, float* o, float* lse, int B,
+                        int H, int H_kv, int N_q, int N_kv, int d, float c_log2, int causal,
+                        int delta, DevCtl ctl, cudaStream_t s) {
+    if (d == 64)
+        return launch_impl<64, false, true>(q, k, v, o, lse, B, H, H_kv, N_q, N_kv, delta, c_log2,
+                                            1.0f, nullptr, nullptr, nullptr, causal, ctl, s);
+    return launch_impl<128, false, true>(q, k, v, o, lse, B, H, H_kv, N_q, N_kv, delta, c_log2,
+                                         1.0f, nullptr, nullptr, nullptr, causal, ctl, s);
 }
 
 }  // namespace fa

@@ -34,6 +34,21 @@ int launch_fwd_sm103(const void* q, const void* k, const void* v, void* o, float
                      const float* kd, const float* vd, int causal, bool is_fp8, DevCtl ctl,
                      cudaStream_t s);
 
+// Forward over one shard of keys, bf16 inputs, d in {64, 128}: N_q queries against
+// N_kv keys; when causal, key j reaches query i iff j <= i + delta (delta = the
+// queries' global offset minus the keys').  O is written as float32 [B*H][N_q][d];
+// rows that reach no key get O = 0 and lse = -inf.
+int launch_fwd_kv_shard(const void* q, const void* k, const void* v, float* o, float* lse, int B,
+                        int H, int H_kv, int N_q, int N_kv, int d, float c_log2, int causal,
+                        int delta, DevCtl ctl, cudaStream_t s);
+
+// Merge of n_parts normalised partial outputs over disjoint key sets:
+// lse = ln sum_s exp(lse_s), O = sum_s exp(lse_s - lse) O_s.  o_parts float32
+// [n_parts][rows][d], lse_parts [n_parts][rows]; o bf16 (o_f32 = 0) or float32
+// [rows][d]; lse (optional) [rows].
+cudaError_t launch_lse_merge(const float* o_parts, const float* lse_parts, int n_parts,
+                             size_t rows, int d, void* o, int o_f32, float* lse, cudaStream_t s);
+
 // Backward pieces.  Workspace layout (all float32, Np = N rounded up to 128):
 //   [0, BH*Np)            -delta_i  (BH = B*H query heads) = -(dO_i . O_i)
 //   [BH*Np, 2*BH*Np)      -lse_i * log2(e)   (both negated for packed FMA/FADD use)

@@ -122,6 +122,49 @@ int fa_fwd_fp8_per_head(const void* q8, const void* k8, const void* v8, void* o,
                         int B, int H, int N, int d, float scale, int causal, void* stream);
 
 /*
+ * Forward over one shard of the keys, the per-shard step of sequence-sharded
+ * attention: N_q queries at global positions q_offset + i against N_kv keys at
+ * global positions kv_offset + j.  It is the forward of "FlashAttention-1",
+ * 10.2.1-10.2.3, on the keys the shard holds; its normalised output and lse are
+ * what fa_lse_merge combines across shards (the two-state combination of 10.2.2).
+ *
+ *   q        : [B][H][N_q][d] bfloat16.   k, v : [B][H_kv][N_kv][d] bfloat16
+ *              (H_kv divides H; query head h reads K/V head h / (H / H_kv)).
+ *   o_part   : [B][H][N_q][d] FLOAT32, written (the shard's normalised output).
+ *   lse_part : [B][H][N_q] float32, written, required.
+ *   causal   : 0, or 1: key j reaches query i iff kv_offset + j <= q_offset + i.
+ *              A row that reaches no key of the shard gets O = 0, lse = -inf.
+ *   dtype    : FA_BF16.  d : 64 or 128.  Offsets are only compared, never used
+ *              to address memory: k and v start at the shard's first key.
+ * Errors: as fa_fwd; FA_ERR_INVALID_ARG also for lse_part null, N_kv < 1, or
+ * H_kv not dividing H.
+ */
+int fa_fwd_kv_shard(const void* q, const void* k, const void* v, float* o_part,
+                    float* lse_part, int B, int H, int H_kv, int N_q, int N_kv, int d,
+                    float scale, int causal, long long q_offset, long long kv_offset,
+                    int dtype, void* stream);
+
+/*
+ * Merge n_parts shard outputs of the same queries over disjoint key sets
+ * ("FlashAttention-1", 10.2.2: partial states combine through their maxima and
+ * sums; with normalised parts the weight of part s is exp(lse_s - lse)):
+ *     lse = ln sum_s exp(lse_s),   O = sum_s exp(lse_s - lse) O_s.
+ * Parts with lse_s = -inf add nothing; a row with every lse_s = -inf gives O = 0
+ * and lse = -inf.  The result equals the forward over the union of the keys up to
+ * rounding.
+ *
+ *   o_parts   : [n_parts][B][H][N][d] float32 (the fa_fwd_kv_shard outputs,
+ *               stacked), read only.   lse_parts : [n_parts][B][H][N] float32.
+ *   o         : [B][H][N][d] written, bfloat16 (dtype FA_BF16) or float32
+ *               (FA_F32).   lse : [B][H][N] float32, written, or NULL.
+ *   d         : 64 or 128.  Every pointer 16-byte aligned.
+ * Errors: FA_ERR_INVALID_ARG (null/misaligned pointers, n_parts < 1, bad sizes or
+ * dtype), FA_ERR_UNSUPPORTED (other d), FA_ERR_CUDA (launch failure).
+ */
+int fa_lse_merge(const float* o_parts, const float* lse_parts, int n_parts, void* o,
+                 float* lse, int B, int H, int N, int d, int dtype, void* stream);
+
+/*
  * Bytes of device workspace that fa_bwd needs for these sizes: the per-row
  * delta_i = dO_i . O_i and the pre-scaled lse (float32, N rounded up to 128
  * per head), plus for d = 64 the float32 dQ accumulator

@@ -122,3 +122,25 @@ def test_bwd_gqa_argument_errors(L):
     assert b(H_kv=3) == 1                # 4 % 3 != 0
     assert b(ws_bytes=ws - 4) == 1
     assert b(d=96) == 2
+
+
+def test_kv_shard_argument_errors(L):
+    def f(lse=P, Nkv=128, H_kv=1, d=64, dtype=1):
+        return L.fa_fwd_kv_shard(P, P, P, P, lse, 1, 2, H_kv, 128, Nkv, d, 0.125, 1, 0, 0, dtype,
+                                 None)
+    assert f(lse=None) == 1            # the merge needs lse
+    assert f(Nkv=0) == 1
+    assert f(H_kv=3) == 1
+    assert f(dtype=0) == 2             # fp32 inputs: not on this path
+    assert f(d=96) == 2
+
+
+def test_lse_merge_argument_errors(L):
+    def m(op=P, lp=P, o=P, S=2, d=64, dtype=1, lse=None):
+        return L.fa_lse_merge(op, lp, S, o, lse, 1, 1, 128, d, dtype, None)
+    assert m(op=None) == 1
+    assert m(lp=MIS) == 1
+    assert m(lse=MIS) == 1
+    assert m(S=0) == 1
+    assert m(dtype=2) == 1
+    assert m(d=32) == 2
