@@ -275,8 +275,12 @@ def make_extra(torch, fa, inputs, ex, dev, stream):
                                fa.FA_BF16, stream)
         mid.record(stream)
         fa.fa_lse_merge(o_p, l_p, o, lse, fa.FA_BF16, stream)
+    # algorithmic bytes of the merge: every part's lse, the O rows of the parts whose
+    # keys a row reached (under the causal mask, key shard t reaches rows >= t*n
+    # only; the rest carry lse = -inf and are not read), the merged O (bf16) and lse
     rows = B * H * N
-    merge_bytes = S * rows * (4 * d + 4) + rows * (2 * d + 4)
+    reached = B * H * (sum(N - t * n for t in range(S)) if causal else S * N)
+    merge_bytes = S * rows * 4 + reached * 4 * d + rows * (2 * d + 4)
     return run, f_fwd, {"mid": mid, "merge_bytes": merge_bytes, "launches": S + 1}
 
 

@@ -215,7 +215,7 @@ __attribute__((visibility("default"))) int fa_lse_merge(const float* o_parts,
     if (lse != nullptr && !aligned16(lse)) return FA_ERR_INVALID_ARG;
     if (n_parts < 1 || B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
     if (dtype != FA_F32 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
-    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if ((d != 64 && d != 128) || n_parts > 16) return FA_ERR_UNSUPPORTED;
     const size_t rows = static_cast<size_t>(B) * H * N;
     if (rows * static_cast<size_t>(n_parts) > (static_cast<size_t>(1) << 40))
         return FA_ERR_UNSUPPORTED;

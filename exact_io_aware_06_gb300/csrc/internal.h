@@ -44,7 +44,7 @@ int launch_fwd_kv_shard(const void* q, const void* k, const void* v, float* o, f
 
 // Merge of n_parts normalised partial outputs over disjoint key sets:
 // lse = ln sum_s exp(lse_s), O = sum_s exp(lse_s - lse) O_s.  o_parts float32
-// [n_parts][rows][d], lse_parts [n_parts][rows]; o bf16 (o_f32 = 0) or float32
+// [n_parts][rows][d], lse_parts [n_parts][rows], n_parts <= 16; o bf16 (o_f32 = 0) or float32
 // [rows][d]; lse (optional) [rows].
 cudaError_t launch_lse_merge(const float* o_parts, const float* lse_parts, int n_parts,
                              size_t rows, int d, void* o, int o_f32, float* lse, cudaStream_t s);

@@ -10,10 +10,10 @@
 // saw no key has lse_s = -inf and weight 0; a row that saw no key in any shard
 // gives O = 0 and lse = -inf.
 //
-// Bandwidth-bound: each partial row is read once (float32), the merged row written
-// once.  A thread owns one float4 of a row (d / 4 threads per row, consecutive
-// threads on consecutive 16-byte pieces of consecutive rows, so every warp reads
-// whole 512-byte row segments); the grid strides over rows.
+// Bandwidth-bound: each partial row that a row's keys reached is read once
+// (float32), the merged row written once.  A lane owns one float4 of a row (d / 4
+// lanes per row, so a warp reads whole 512-byte row segments); the grid strides
+// over rows.
 #include <cmath>
 
 #include "internal.h"
@@ -22,45 +22,68 @@
 namespace fa {
 namespace {
 
+constexpr int kMaxParts = 16;  // parts per merge (a lane per part for the lse reduction)
+
+// A row is owned by a group of D/4 lanes (one float4 each: the whole row); lane j of
+// the group reads lse of part j, the group reduces max and sum with shuffles, and
+// every lane then reads its float4 of each part that the row's keys reached, four
+// parts' loads in flight at a time.
 template <int D, bool OUT_F32>
 __global__ void __launch_bounds__(256)
     lse_merge_kernel(const float4* __restrict__ o_parts, const float* __restrict__ lse_parts,
                      int n_parts, size_t rows, void* __restrict__ o, float* __restrict__ lse) {
-    constexpr int kVec = D / 4;  // float4 pieces per row
-    const size_t units = rows * kVec;
-    const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
-    for (size_t x = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; x < units;
-         x += stride) {
-        const size_t row = x / kVec;
-        const int c = static_cast<int>(x % kVec);
-        float m = -INFINITY;
-        for (int s = 0; s < n_parts; ++s) m = fmaxf(m, __ldg(lse_parts + s * rows + row));
+    constexpr int kVec = D / 4;         // lanes per row
+    constexpr int kGroups = 32 / kVec;  // rows per warp
+    static_assert(kVec >= kMaxParts, "a lane per part");
+    const int lane = threadIdx.x & 31, j = lane % kVec, g = lane / kVec;
+    const size_t warp = (static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
+    const size_t step = static_cast<size_t>(gridDim.x) * blockDim.x / 32 * kGroups;
+    // the loop bound is the warp's first row, so whole warps iterate together
+    for (size_t row = warp * kGroups + g; row - g < rows; row += step) {
+        const bool in = row < rows;
+        const float l = (in && j < n_parts) ? __ldg(lse_parts + j * rows + row) : -INFINITY;
+        float m = l;
+#pragma unroll
+        for (int off = kVec / 2; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+        const float w = (l == -INFINITY) ? 0.f : expf(l - m);  // exp(lse_j - max), 0 if unreached
+        float tot = w;
+#pragma unroll
+        for (int off = kVec / 2; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        float out_lse = -INFINITY;
-        if (m != -INFINITY) {
-            float tot = 0.f;
-            for (int s = 0; s < n_parts; ++s) tot += expf(__ldg(lse_parts + s * rows + row) - m);
-            const float inv = 1.f / tot;
-#pragma unroll 4
-            for (int s = 0; s < n_parts; ++s) {
-                const float l = __ldg(lse_parts + s * rows + row);
-                if (l == -INFINITY) continue;  // no key of this shard reached the row
-                const float w = expf(l - m) * inv;
-                const float4 v = __ldcs(o_parts + (s * rows + row) * kVec + c);
-                acc.x = fmaf(w, v.x, acc.x);
-                acc.y = fmaf(w, v.y, acc.y);
-                acc.z = fmaf(w, v.z, acc.z);
-                acc.w = fmaf(w, v.w, acc.w);
+#pragma unroll
+        for (int s0 = 0; s0 < kMaxParts; s0 += 4) {
+            if (s0 >= n_parts) break;  // uniform across the warp
+            float ws[4];
+            float4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                ws[u] = __shfl_sync(0xffffffffu, w, g * kVec + s0 + u);  // 0 past n_parts
+                v[u] = (ws[u] != 0.f) ? __ldcs(o_parts + ((s0 + u) * rows + row) * kVec + j)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
             }
-            out_lse = m + logf(tot);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                acc.x = fmaf(ws[u], v[u].x, acc.x);
+                acc.y = fmaf(ws[u], v[u].y, acc.y);
+                acc.z = fmaf(ws[u], v[u].z, acc.z);
+                acc.w = fmaf(ws[u], v[u].w, acc.w);
+            }
         }
-        if (OUT_F32) {
-            reinterpret_cast<float4*>(o)[row * kVec + c] = acc;
-        } else {
-            reinterpret_cast<uint2*>(o)[row * kVec + c] =
-                make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+        if (in) {
+            const bool any = m != -INFINITY;
+            const float inv = any ? 1.f / tot : 0.f;  // tot >= 1 when any part was reached
+            acc.x *= inv;
+            acc.y *= inv;
+            acc.z *= inv;
+            acc.w *= inv;
+            if (OUT_F32) {
+                reinterpret_cast<float4*>(o)[row * kVec + j] = acc;
+            } else {
+                reinterpret_cast<uint2*>(o)[row * kVec + j] =
+                    make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+            }
+            if (lse != nullptr && j == 0) lse[row] = any ? m + logf(tot) : -INFINITY;
         }
-        if (lse != nullptr && c == 0) lse[row] = out_lse;
     }
 }
 
@@ -70,9 +93,14 @@ cudaError_t launch_merge_impl(const float* o_parts, const float* lse_parts, int 
     int sms = 152, dev = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const size_t units = rows * (D / 4);
-    size_t blocks = (units + 255) / 256;
-    const size_t cap = static_cast<size_t>(sms) * 8;  // 8 blocks of 256 threads per SM
+    // one full wave of resident blocks; the grid strides over the rest
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, lse_merge_kernel<D, OUT_F32>, 256,
+                                                      0) != cudaSuccess || per_sm < 1)
+        per_sm = 4;
+    const size_t warps_needed = (rows + (128 / D) - 1) / (128 / D);
+    size_t blocks = (warps_needed + 7) / 8;
+    const size_t cap = static_cast<size_t>(sms) * per_sm;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     lse_merge_kernel<D, OUT_F32><<<static_cast<unsigned>(blocks), 256, 0, s>>>(

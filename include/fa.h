@@ -157,9 +157,9 @@ int fa_fwd_kv_shard(const void* q, const void* k, const void* v, float* o_part,
  *               stacked), read only.   lse_parts : [n_parts][B][H][N] float32.
  *   o         : [B][H][N][d] written, bfloat16 (dtype FA_BF16) or float32
  *               (FA_F32).   lse : [B][H][N] float32, written, or NULL.
- *   d         : 64 or 128.  Every pointer 16-byte aligned.
+ *   n_parts   : 1 to 16.   d : 64 or 128.  Every pointer 16-byte aligned.
  * Errors: FA_ERR_INVALID_ARG (null/misaligned pointers, n_parts < 1, bad sizes or
- * dtype), FA_ERR_UNSUPPORTED (other d), FA_ERR_CUDA (launch failure).
+ * dtype), FA_ERR_UNSUPPORTED (other d, n_parts > 16), FA_ERR_CUDA (launch failure).
  */
 int fa_lse_merge(const float* o_parts, const float* lse_parts, int n_parts, void* o,
                  float* lse, int B, int H, int N, int d, int dtype, void* stream);

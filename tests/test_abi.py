@@ -144,3 +144,4 @@ def test_lse_merge_argument_errors(L):
     assert m(S=0) == 1
     assert m(dtype=2) == 1
     assert m(d=32) == 2
+    assert m(S=17) == 2

@@ -88,7 +88,7 @@ def random_parts(S, B, H, N, d, seed, with_empty=True):
     return o, lse
 
 
-@pytest.mark.parametrize("S", [1, 2, 3, 5])
+@pytest.mark.parametrize("S", [1, 2, 3, 5, 16])
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("out", ["f32", "bf16"])
 def test_lse_merge_against_oracle(S, d, out):
