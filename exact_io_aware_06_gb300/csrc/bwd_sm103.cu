@@ -22,7 +22,9 @@
 //   warp 1      MMA issuer + TMEM owner
 //   warps 4-7   P/dS for query columns 0-63 of block i   (thread = key row)
 //   warps 8-11  P/dS for query columns 64-127
-//   warps 12-15 drain dQ_i from TMEM into the fp32 accumulator (vector atomics)
+//   warps 12-15 drain dQ_i from TMEM into the fp32 accumulator: each warp stages its
+//               32 rows in the dS buffer that dQ_i has just consumed (128-byte
+//               swizzled boxes) and adds them with TMA bulk tensor reductions
 //   TMEM: S^T 0-127 (P^T bf16 over 0-31 and 64-95), dP^T 128-255 (dS^T bf16 over
 //         128-159 and 192-223: each half writes only inside the columns it read),
 //         dV 256-319, dK 320-383, dQ double buffer 384-447 / 448-511.
@@ -45,7 +47,29 @@ namespace {
 constexpr int kBlk = 128;            // keys per CTA, queries per inner step
 constexpr float kLog2e = 1.4426950408889634f;
 
-// d = 64: dK, dV and dQ in one kernel (dQ partials through fp32 vector atomics).
+// Add a (32 x 32 fp32) box from shared memory into global memory through the
+// tensor map (TMA reduction, f32 add), tracked by the thread's bulk async-group.
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, uint32_t src, int x, int y,
+                                                  int z) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group"
+        " [%0, {%2, %3, %4}], [%1];" ::"l"(reinterpret_cast<uint64_t>(map)),
+        "r"(src), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// All of this thread's committed bulk operations have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// All of this thread's committed bulk operations have completed.
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// d = 64: dK, dV and dQ in one kernel (dQ partials added by TMA bulk reductions).
 // d = 128: TMEM holds S^T, dP^T, dV and dK (4 x 128 columns) and nothing else, so
 // this kernel computes dK and dV only; bwd_dq_kernel computes dQ.
 template <int D>
@@ -110,6 +134,7 @@ template <int D>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const __grid_constant__ CUtensorMap tm_dq,
                     const BwdArgs args) {
     using C = BwdCfg<D>;
     constexpr int kD = D, kQStages = C::kQStages, kTile = C::kTile, kChunks = C::kChunks;
@@ -153,7 +178,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             mbar_init(smem_u32(&bars.q_empty[s]), 1);
         }
         for (int s = 0; s < 2; ++s) {
-            mbar_init(smem_u32(&bars.ds_empty[s]), 1);
+            mbar_init(smem_u32(&bars.ds_empty[s]), 4);  // the four dQ drain warps
             mbar_init(smem_u32(&bars.dq_full[s]), 1);
             mbar_init(smem_u32(&bars.dq_free[s]), 128);
         }
@@ -170,6 +195,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
         tma_prefetch_desc(&tm_do);
+        if (C::kFusedDQ) tma_prefetch_desc(&tm_dq);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(&tmem_slot), kTmemCols);
@@ -253,25 +279,29 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                 const int s1 = (i + 1) % kQStages;
                 const bool more = i + 1 < n_it;
                 const uint32_t sQ = sb + kOffQ + s * kTile, sDO = sb + kOffDO + s * kTile;
-                // dV += P^T dO_i
+                // Two wait points per block.  A wait issued behind queued MMAs costs the
+                // time those MMAs take to enter the tensor pipe, however long ago the
+                // phase completed; a second wait right after it is cheap.  So the loads
+                // of block i+1 (ready blocks ahead) are checked together with P_i, and
+                // the dQ buffer (freed blocks ahead) together with dS_i.
                 ok = mbar_wait(smem_u32(&bars.p_full), i & 1, lim, &abort_flag);
+                if (ok && more)
+                    ok = mbar_wait(smem_u32(&bars.q_full[s1]), ((i + 1) / kQStages) & 1, lim, &abort_flag);
                 if (!ok) break;
                 tc_fence_after();
+                // dV += P^T dO_i
 #pragma unroll
                 for (int kk = 0; kk < kBlk / 16; ++kk)
                     mma_bf16_ts(tmem + kColDV, tmem + kColS + 64 * (kk >> 2) + 8 * (kk & 3),
                                 sdesc_sw128(sDO + 2048 * kk, 16384, 1024), kIdescTS, (i > 0) || (kk > 0));
                 // next block's scores: the P/dS warps keep P_i in registers
-                if (more) {
-                    ok = mbar_wait(smem_u32(&bars.q_full[s1]), ((i + 1) / kQStages) & 1, lim, &abort_flag);
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_s(s1);
-                }
-                // dK += dS^T Q_i
+                if (more) issue_s(s1);
                 ok = mbar_wait(smem_u32(&bars.ds_full), i & 1, lim, &abort_flag);
+                if (C::kFusedDQ && ok && i >= 2)
+                    ok = mbar_wait(smem_u32(&bars.dq_free[i & 1]), ((i >> 1) & 1) ^ 1, lim, &abort_flag);
                 if (!ok) break;
                 tc_fence_after();
+                // dK += dS^T Q_i
 #pragma unroll
                 for (int kk = 0; kk < kBlk / 16; ++kk)
                     mma_bf16_ts(tmem + kColDK, tmem + kColDP + 64 * (kk >> 2) + 8 * (kk & 3),
@@ -281,18 +311,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                 if constexpr (C::kFusedDQ) {
                     // dQ_i = dS_i K_j into TMEM buffer i % 2
                     const int b = i & 1;
-                    if (i >= 2) {
-                        ok = mbar_wait(smem_u32(&bars.dq_free[b]), ((i >> 1) & 1) ^ 1, lim, &abort_flag);
-                        if (!ok) break;
-                        tc_fence_after();
-                    }
                     const uint32_t sDS = sb + kOffDS + b * kDSBytes;
 #pragma unroll
                     for (int kk = 0; kk < kBlk / 16; ++kk)
                         mma_bf16_ss(tmem + kColDQ + 64 * b, sdesc_sw128(sDS + 2048 * kk, 16384, 1024),
                                     sdesc_sw128(sK + 2048 * kk, 16384, 1024), kIdescDQ, kk > 0);
-                    mma_commit(smem_u32(&bars.dq_full[b]));
-                    mma_commit(smem_u32(&bars.ds_empty[b]));
+                    mma_commit(smem_u32(&bars.dq_full[b]));  // also: dS buffer b consumed
                 }
             }
             if (ok) mma_commit(smem_u32(&bars.all_done));
@@ -420,6 +444,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         }
     } else if (C::kFusedDQ && warp >= 12) {
         // ================================================================ dQ drain
+        // dQ_i (fp32, TMEM) -> this warp's 32 rows staged in dS buffer b, which the dQ_i
+        // MMA has finished reading once dq_full[b] completes -> two TMA reductions
+        // (32 rows x 32 columns each) into the accumulator.  The staging uses the
+        // 128-byte swizzle of the tensor map (16-byte chunk c of row r at chunk
+        // c ^ (r % 8)), so the 32 lanes' row writes hit distinct banks.  Buffer b is
+        // handed back to the P/dS warps (ds_empty[b]) once the reductions have read it.
         const int wq = warp % 4;
         const int row_in_blk = wq * 32 + lane;
         const uint32_t lb = tmem + (static_cast<uint32_t>(wq * 32) << 16);
@@ -435,17 +465,31 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             tmem_ld32(lb + kColDQ + 64 * b + 32, r[1]);
             tc_fence_before();
             mbar_arrive(smem_u32(&bars.dq_free[b]));
-            float* acc = args.dq_acc +
-                         (static_cast<size_t>(q_head(i)) * Np + static_cast<size_t>(q_blk(i)) * kBlk + row_in_blk) * kD;
+            const uint32_t box0 = sb + kOffDS + b * kDSBytes + wq * 8192;  // two 4 KB boxes
 #pragma unroll
             for (int h = 0; h < 2; ++h)
 #pragma unroll
-                for (int x = 0; x < 8; ++x)
-                    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(acc + 32 * h + 4 * x),
-                                 "f"(__uint_as_float(r[h][4 * x])), "f"(__uint_as_float(r[h][4 * x + 1])),
-                                 "f"(__uint_as_float(r[h][4 * x + 2])), "f"(__uint_as_float(r[h][4 * x + 3]))
+                for (int c = 0; c < 8; ++c) {
+                    const uint32_t dst = box0 + h * 4096 + lane * 128 + ((c ^ (lane & 7)) << 4);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst),
+                                 "r"(r[h][4 * c]), "r"(r[h][4 * c + 1]), "r"(r[h][4 * c + 2]),
+                                 "r"(r[h][4 * c + 3])
                                  : "memory");
+                }
+            fence_proxy_async_smem();  // generic-proxy writes -> visible to the TMA unit
+            __syncwarp();
+            if (lane == 0) {
+                const int y = q_blk(i) * kBlk + wq * 32;
+                tma_reduce_add_3d(&tm_dq, box0, 0, y, q_head(i));
+                tma_reduce_add_3d(&tm_dq, box0 + 4096, 32, y, q_head(i));
+                bulk_commit_group();
+                bulk_wait_read_all();
+                mbar_arrive(smem_u32(&bars.ds_empty[b]));
+            }
+            __syncwarp();
         }
+        // the reductions must complete before the CTA's shared memory goes away
+        if (lane == 0) bulk_wait_all();
         if (!ok && lane == 0) record_timeout(args.ctl, &abort_flag);
     }
 
@@ -561,6 +605,10 @@ int launch_bwd_impl(const void* q, const void* k, const void* v, const void* o, 
     if (rc == 0) rc = make_map_3d(&tk, k, dt, 2, D, N, BH_kv, 64, kBlk);
     if (rc == 0) rc = make_map_3d(&tv, v, dt, 2, D, N, BH_kv, 64, kBlk);
     if (rc == 0) rc = make_map_3d(&tdo, dO, dt, 2, D, N, BH, 64, kBlk);
+    // fp32 accumulator [BH][Np][64], reduced into in 32 x 32 boxes (fused dQ only)
+    CUtensorMap tdq = tq;
+    if (rc == 0 && C::kFusedDQ)
+        rc = make_map_3d(&tdq, dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, Np, BH, 32, 32);
     if (rc != 0) return rc;
     static uint64_t attr_set = 0;
     if (dev >= 64 || !(attr_set & (1ull << dev))) {
@@ -585,7 +633,7 @@ int launch_bwd_impl(const void* q, const void* k, const void* v, const void* o, 
     a.c_log2 = scale * kLog2e;
     a.scale = scale;
     a.ctl = ctl;
-    bwd_main_kernel<D><<<a.n_kv * BH_kv, C::kThreads, C::kSmemAlloc, s>>>(tq, tk, tv, tdo, a);
+    bwd_main_kernel<D><<<a.n_kv * BH_kv, C::kThreads, C::kSmemAlloc, s>>>(tq, tk, tv, tdo, tdq, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return static_cast<int>(e);
 

@@ -59,10 +59,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0u;
 }
 
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0u;
+}
+
 // Wait for the phase with the given parity to complete.  Returns false when
 // `*abort` becomes non-zero or when more than `limit_ns` elapse; true otherwise.
+// A phase that has already completed is detected with the non-blocking test: a
+// try_wait issued while the thread's tensor-core instructions are still queued
+// costs a few hundred cycles even when it succeeds at once.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns,
                                           const volatile int* abort) {
+    if (mbar_test_wait(bar, parity)) return true;
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
         if (mbar_try_wait(bar, parity)) return true;
