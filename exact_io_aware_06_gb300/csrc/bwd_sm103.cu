@@ -19,7 +19,8 @@
 //
 // bwd_main layout (d = 64), 16 warps:
 //   warp 0      TMA producer: K_j, V_j once; Q_i, dO_i, lse_i, delta_i in a 3-stage ring
-//   warp 1      MMA issuer + TMEM owner
+//   warp 1      MMA issuer (dV, S, dK, dP) + TMEM owner
+//   warp 2      second MMA issuer: dQ (d = 64 only)
 //   warps 4-7   P/dS for query columns 0-63 of block i   (thread = key row)
 //   warps 8-11  P/dS for query columns 64-127
 //   warps 12-15 drain dQ_i from TMEM into the fp32 accumulator: each warp stages its
@@ -33,7 +34,7 @@
 //     S^T  = K_j Q_{i+1}^T    (SS, both K-major)           P_i lives on in registers
 //     dK  += dS^T Q_i         (TS, Q_i MN-major)           after dS_i is in TMEM/smem
 //     dP^T = V_j dO_{i+1}^T   (SS, both K-major)
-//     dQ_i = dS_i K_j         (SS, dS from smem MN-major, K_j MN-major)
+//     dQ_i = dS_i K_j         (SS, dS from smem MN-major, K_j MN-major; warp 2)
 //   so the next block's scores are ready when the P/dS warps finish dS_i.
 #include <cmath>
 
@@ -118,11 +119,12 @@ template <int NQ>
 struct Bars {
     uint64_t kv_full;
     uint64_t q_full[NQ], q_empty[NQ];
-    uint64_t s_full, dp_full, p_full, ds_full;
+    uint64_t s_full, dp_full, p_full;
+    uint64_t ds_full[2];  // dS_i written (TMEM and dS buffer i % 2); one barrier per buffer
     uint64_t ds_empty[2];
     uint64_t dq_full[2], dq_free[2];
     uint64_t all_done;
-    uint64_t drain;
+    uint64_t drain, drain2;
 };
 
 __device__ __forceinline__ void record_timeout(const DevCtl& ctl, volatile int* abort_flag) {
@@ -185,9 +187,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         mbar_init(smem_u32(&bars.s_full), 1);
         mbar_init(smem_u32(&bars.dp_full), 1);
         mbar_init(smem_u32(&bars.p_full), 256);
-        mbar_init(smem_u32(&bars.ds_full), 256);
+        mbar_init(smem_u32(&bars.ds_full[0]), 256);
+        mbar_init(smem_u32(&bars.ds_full[1]), 256);
         mbar_init(smem_u32(&bars.all_done), 1);
         mbar_init(smem_u32(&bars.drain), 1);
+        mbar_init(smem_u32(&bars.drain2), 1);
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
@@ -279,11 +283,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                 const int s1 = (i + 1) % kQStages;
                 const bool more = i + 1 < n_it;
                 const uint32_t sQ = sb + kOffQ + s * kTile, sDO = sb + kOffDO + s * kTile;
-                // Two wait points per block.  A wait issued behind queued MMAs costs the
-                // time those MMAs take to enter the tensor pipe, however long ago the
-                // phase completed; a second wait right after it is cheap.  So the loads
-                // of block i+1 (ready blocks ahead) are checked together with P_i, and
-                // the dQ buffer (freed blocks ahead) together with dS_i.
+                // The loads of block i+1 (ready blocks ahead) are checked together with
+                // P_i: every wait of an issuing thread can leave the tensor pipe idle.
                 ok = mbar_wait(smem_u32(&bars.p_full), i & 1, lim, &abort_flag);
                 if (ok && more)
                     ok = mbar_wait(smem_u32(&bars.q_full[s1]), ((i + 1) / kQStages) & 1, lim, &abort_flag);
@@ -296,9 +297,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                                 sdesc_sw128(sDO + 2048 * kk, 16384, 1024), kIdescTS, (i > 0) || (kk > 0));
                 // next block's scores: the P/dS warps keep P_i in registers
                 if (more) issue_s(s1);
-                ok = mbar_wait(smem_u32(&bars.ds_full), i & 1, lim, &abort_flag);
-                if (C::kFusedDQ && ok && i >= 2)
-                    ok = mbar_wait(smem_u32(&bars.dq_free[i & 1]), ((i >> 1) & 1) ^ 1, lim, &abort_flag);
+                // one barrier per dS buffer: writing buffer i % 2 again needs block i's
+                // dK and dQ, so no waiter can fall two phases behind
+                ok = mbar_wait(smem_u32(&bars.ds_full[i & 1]), (i >> 1) & 1, lim, &abort_flag);
                 if (!ok) break;
                 tc_fence_after();
                 // dK += dS^T Q_i
@@ -308,22 +309,41 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                                 sdesc_sw128(sQ + 2048 * kk, 16384, 1024), kIdescTS, (i > 0) || (kk > 0));
                 mma_commit(smem_u32(&bars.q_empty[s]));  // Q_i, dO_i, lse_i, delta_i consumed
                 if (more) issue_dp(s1);
-                if constexpr (C::kFusedDQ) {
-                    // dQ_i = dS_i K_j into TMEM buffer i % 2
-                    const int b = i & 1;
-                    const uint32_t sDS = sb + kOffDS + b * kDSBytes;
-#pragma unroll
-                    for (int kk = 0; kk < kBlk / 16; ++kk)
-                        mma_bf16_ss(tmem + kColDQ + 64 * b, sdesc_sw128(sDS + 2048 * kk, 16384, 1024),
-                                    sdesc_sw128(sK + 2048 * kk, 16384, 1024), kIdescDQ, kk > 0);
-                    mma_commit(smem_u32(&bars.dq_full[b]));  // also: dS buffer b consumed
-                }
             }
             if (ok) mma_commit(smem_u32(&bars.all_done));
             if (!ok) record_timeout(args.ctl, &abort_flag);
             mma_commit(smem_u32(&bars.drain));
             const volatile int never = 0;
             mbar_wait(smem_u32(&bars.drain), 0, kDrainWaitNs, &never);
+        }
+    } else if (C::kFusedDQ && warp == 2) {
+        // ================================================================ dQ MMA issuer
+        // dQ_i = dS_i K_j (dS from its shared-memory buffer i % 2, K MN-major) into TMEM
+        // buffer i % 2.  A second issuing thread: its waits (dS_i, the dQ buffer) do not
+        // stall the main MMA chain, and its MMAs read nothing that chain writes (dS in
+        // shared memory, K) and write only the dQ buffers.
+        if (lane == 0) {
+            const uint32_t sK = sb + kOffK;
+            bool ok = mbar_wait(smem_u32(&bars.kv_full), 0, lim, &abort_flag);
+            for (int i = 0; i < n_it && ok; ++i) {
+                const int b = i & 1;
+                ok = mbar_wait(smem_u32(&bars.ds_full[b]), (i >> 1) & 1, lim, &abort_flag);
+                if (ok && i >= 2)
+                    ok = mbar_wait(smem_u32(&bars.dq_free[b]), ((i >> 1) & 1) ^ 1, lim, &abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t sDS = sb + kOffDS + b * kDSBytes;
+#pragma unroll
+                for (int kk = 0; kk < kBlk / 16; ++kk)
+                    mma_bf16_ss(tmem + kColDQ + 64 * b, sdesc_sw128(sDS + 2048 * kk, 16384, 1024),
+                                sdesc_sw128(sK + 2048 * kk, 16384, 1024), kIdescDQ, kk > 0);
+                mma_commit(smem_u32(&bars.dq_full[b]));  // also: dS buffer b consumed
+            }
+            if (!ok) record_timeout(args.ctl, &abort_flag);
+            // drain this thread's MMAs before TMEM is released
+            mma_commit(smem_u32(&bars.drain2));
+            const volatile int never = 0;
+            mbar_wait(smem_u32(&bars.drain2), 0, kDrainWaitNs, &never);
         }
     } else if (warp >= 4 && warp < 12) {
         static_assert(C::kThreads >= 384, "P/dS warpgroups are warps 4-11");
@@ -410,7 +430,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             tmem_st_wait();
             if constexpr (C::kFusedDQ) fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(smem_u32(&bars.ds_full));
+            mbar_arrive(smem_u32(&bars.ds_full[i & 1]));
         }
         // epilogue: warps 4-7 store dV, warps 8-11 store dK (times scale)
         if (ok) {
