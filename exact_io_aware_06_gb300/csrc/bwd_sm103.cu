@@ -11,10 +11,11 @@
 // Three kernels on one stream:
 //   1. bwd_prep      delta_i (fp32), lse_i * log2(e) copied into a padded
 //                    workspace row, and the fp32 dQ accumulator zeroed.
-//   2. bwd_main      one CTA per (head, 128-key block j), looping over all
-//                    128-row query blocks i; dK_j and dV_j accumulate in TMEM
-//                    for the whole loop, dQ_i partials go to the fp32
-//                    accumulator with vector atomics.
+//   2. bwd_main      persistent, one CTA per SM working through (head, 128-key
+//                    block j) items; per item it loops over all 128-row query
+//                    blocks i, dK_j and dV_j accumulate in TMEM
+//                    for the whole loop, dQ_i partials are added to the fp32
+//                    accumulator by TMA bulk tensor reductions (d = 64).
 //   3. bwd_dq_convert  dQ = bf16(scale * accumulator).
 //
 // bwd_main layout (d = 64), 16 warps:
@@ -117,7 +118,7 @@ struct BwdArgs {
 
 template <int NQ>
 struct Bars {
-    uint64_t kv_full;
+    uint64_t kv_full, kv_empty;  // the K/V tile of the current item
     uint64_t q_full[NQ], q_empty[NQ];
     uint64_t s_full, dp_full, p_full;
     uint64_t ds_full[2];  // dS_i written (TMEM and dS buffer i % 2); one barrier per buffer
@@ -153,28 +154,41 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const uint32_t sb = (smem_u32(smem_raw) + 1023u) & ~1023u;
     uint8_t* const sb_ptr = smem_raw + (sb - smem_u32(smem_raw));
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    // causal: the key block with the most query blocks (kvb = 0) goes first for every head
-    const int bh = args.causal ? static_cast<int>(blockIdx.x % args.BH) : static_cast<int>(blockIdx.x / args.n_kv);
-    const int kvb = args.causal ? static_cast<int>(blockIdx.x / args.BH) : static_cast<int>(blockIdx.x % args.n_kv);
     const int N = args.N, Np = args.Np;
     const int n_q = Np / kBlk;
-    // query blocks this key block meets: all of them, or (causal) blocks kvb..n_q-1.
-    // Loops run over a sweep index (barrier phases, stages, buffers); q_blk() and
-    // q_head() below map it to the query block and query head.
-    const int i0 = args.causal ? kvb : 0;
-    const int n_loc = n_q - i0;
-    // grouped-query attention: this K/V head (bh) serves G query heads, and its dK, dV
-    // sum over all of them.  The sweep runs over it = g * n_loc + i for every query
-    // head g of the group; with H_kv = H it is the plain sweep.
     const int G = args.H / args.H_kv;
-    const int n_it = G * n_loc;
-    auto q_head = [&](int it) { return (bh / args.H_kv) * args.H + (bh % args.H_kv) * G + it / n_loc; };
-    auto q_blk = [&](int it) { return i0 + it % n_loc; };
+    // Persistent: this CTA works through items x = blockIdx.x, + gridDim.x, ... where an
+    // item is one (K/V head bh, 128-key block kvb).  Causal items go heaviest first
+    // (kvb = 0 meets every query block).  Every role walks the same item sequence and
+    // numbers the query blocks g = 0, 1, 2, ... across items: stages and barrier
+    // phases follow g, the K/V tile and the dK/dV accumulators follow the item count.
+    const int n_items = args.n_kv * args.BH;
+    struct Item {
+        int bh, kvb, i0, n_loc, n_it;
+    };
+    auto item_at = [&](int x) {
+        Item I;
+        I.bh = args.causal ? x % args.BH : x / args.n_kv;
+        I.kvb = args.causal ? x / args.BH : x % args.n_kv;
+        // query blocks this key block meets: all of them, or (causal) blocks kvb..n_q-1;
+        // with grouped-query attention, that range for each of the G query heads that
+        // share this K/V head (dK, dV sum over all of them)
+        I.i0 = args.causal ? I.kvb : 0;
+        I.n_loc = n_q - I.i0;
+        I.n_it = G * I.n_loc;
+        return I;
+    };
+    auto q_head = [&](const Item& I, int it) {
+        return (I.bh / args.H_kv) * args.H + (I.bh % args.H_kv) * G + it / I.n_loc;
+    };
+    auto q_blk = [&](const Item& I, int it) { return I.i0 + it % I.n_loc; };
     const uint64_t lim = args.ctl.wait_ns;
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
         mbar_init(smem_u32(&bars.kv_full), 1);
+        // the K/V tile is free again once every thread that reads it has committed
+        mbar_init(smem_u32(&bars.kv_empty), C::kFusedDQ ? 2 : 1);
         for (int s = 0; s < kQStages; ++s) {
             mbar_init(smem_u32(&bars.q_full[s]), 1);
             mbar_init(smem_u32(&bars.q_empty[s]), 1);
@@ -214,38 +228,45 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         // ================================================================ producer
         if (lane == 0) {
             const uint32_t kvf = smem_u32(&bars.kv_full);
-            mbar_arrive_expect_tx(kvf, 2 * kTile);
-            for (int c = 0; c < kChunks; ++c) {  // 64-column swizzle chunks, 16 KB apart
-                tma_load_3d(sb + kOffK + c * 16384, &tm_k, kvf, 64 * c, kvb * kBlk, bh);
-                tma_load_3d(sb + kOffV + c * 16384, &tm_v, kvf, 64 * c, kvb * kBlk, bh);
-            }
-            int issued = 0;
+            int g = 0, kc = 0;
             bool ok = true;
-            for (int i = 0; i < n_it; ++i) {
-                const int s = i % kQStages;
-                const int qb = q_blk(i), qh = q_head(i);
-                if (i >= kQStages &&
-                    !mbar_wait(smem_u32(&bars.q_empty[s]), ((i / kQStages) & 1) ^ 1, lim, &abort_flag)) {
+            for (int x = blockIdx.x; x < n_items && ok; x += gridDim.x, ++kc) {
+                const Item I = item_at(x);
+                // this item's K/V over the previous item's, once that one is consumed
+                if (kc > 0 && !mbar_wait(smem_u32(&bars.kv_empty), (kc - 1) & 1, lim, &abort_flag)) {
                     ok = false;
                     break;
                 }
-                const uint32_t qf = smem_u32(&bars.q_full[s]);
-                mbar_arrive_expect_tx(qf, 2 * kTile + 2 * kBlk * 4);
-                for (int c = 0; c < kChunks; ++c) {
-                    tma_load_3d(sb + kOffQ + s * kTile + c * 16384, &tm_q, qf, 64 * c, qb * kBlk, qh);
-                    tma_load_3d(sb + kOffDO + s * kTile + c * 16384, &tm_do, qf, 64 * c, qb * kBlk, qh);
+                mbar_arrive_expect_tx(kvf, 2 * kTile);
+                for (int c = 0; c < kChunks; ++c) {  // 64-column swizzle chunks, 16 KB apart
+                    tma_load_3d(sb + kOffK + c * 16384, &tm_k, kvf, 64 * c, I.kvb * kBlk, I.bh);
+                    tma_load_3d(sb + kOffV + c * 16384, &tm_v, kvf, 64 * c, I.kvb * kBlk, I.bh);
                 }
-                const size_t row = static_cast<size_t>(qh) * Np + static_cast<size_t>(qb) * kBlk;
-                bulk_load(sb + kOffL + s * kBlk * 4, args.ws_lse2 + row, kBlk * 4, qf);
-                bulk_load(sb + kOffDelta + s * kBlk * 4, args.ws_delta + row, kBlk * 4, qf);
-                issued = i + 1;
+                for (int i = 0; i < I.n_it; ++i, ++g) {
+                    const int s = g % kQStages;
+                    const int qb = q_blk(I, i), qh = q_head(I, i);
+                    if (g >= kQStages &&
+                        !mbar_wait(smem_u32(&bars.q_empty[s]), ((g / kQStages) & 1) ^ 1, lim, &abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t qf = smem_u32(&bars.q_full[s]);
+                    mbar_arrive_expect_tx(qf, 2 * kTile + 2 * kBlk * 4);
+                    for (int c = 0; c < kChunks; ++c) {
+                        tma_load_3d(sb + kOffQ + s * kTile + c * 16384, &tm_q, qf, 64 * c, qb * kBlk, qh);
+                        tma_load_3d(sb + kOffDO + s * kTile + c * 16384, &tm_do, qf, 64 * c, qb * kBlk, qh);
+                    }
+                    const size_t row = static_cast<size_t>(qh) * Np + static_cast<size_t>(qb) * kBlk;
+                    bulk_load(sb + kOffL + s * kBlk * 4, args.ws_lse2 + row, kBlk * 4, qf);
+                    bulk_load(sb + kOffDelta + s * kBlk * 4, args.ws_delta + row, kBlk * 4, qf);
+                }
             }
             if (!ok) record_timeout(args.ctl, &abort_flag);
+            // drain: the newest K/V load and the newest load of every stage have landed
             const volatile int never = 0;
-            mbar_wait(kvf, 0, kDrainWaitNs, &never);
-            for (int i = max(0, issued - kQStages); i < issued; ++i)
-                mbar_wait(smem_u32(&bars.q_full[i % kQStages]), (i / kQStages) & 1, kDrainWaitNs,
-                          &never);
+            if (kc > 0) mbar_wait(kvf, (kc - 1) & 1, kDrainWaitNs, &never);
+            for (int q = max(0, g - kQStages); q < g; ++q)
+                mbar_wait(smem_u32(&bars.q_full[q % kQStages]), (q / kQStages) & 1, kDrainWaitNs, &never);
         }
     } else if (warp == 1) {
         // ================================================================ MMA issuer
@@ -271,46 +292,58 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                 }
                 mma_commit(smem_u32(&bars.dp_full));
             };
-            bool ok = mbar_wait(smem_u32(&bars.kv_full), 0, lim, &abort_flag);
-            if (ok) ok = mbar_wait(smem_u32(&bars.q_full[0]), 0, lim, &abort_flag);
-            if (ok) {
-                tc_fence_after();
-                issue_s(0);
-                issue_dp(0);
-            }
-            for (int i = 0; i < n_it && ok; ++i) {
-                const int s = i % kQStages;
-                const int s1 = (i + 1) % kQStages;
-                const bool more = i + 1 < n_it;
-                const uint32_t sQ = sb + kOffQ + s * kTile, sDO = sb + kOffDO + s * kTile;
-                // The loads of block i+1 (ready blocks ahead) are checked together with
-                // P_i: every wait of an issuing thread can leave the tensor pipe idle.
-                ok = mbar_wait(smem_u32(&bars.p_full), i & 1, lim, &abort_flag);
-                if (ok && more)
-                    ok = mbar_wait(smem_u32(&bars.q_full[s1]), ((i + 1) / kQStages) & 1, lim, &abort_flag);
+            int g = 0, kc = 0;
+            bool ok = true;
+            for (int x = blockIdx.x; x < n_items && ok; x += gridDim.x, ++kc) {
+                const Item I = item_at(x);
+                // the item's first scores; S and dP of the previous item's last block were
+                // read by its dV and dK, issued before these by this thread
+                ok = mbar_wait(smem_u32(&bars.kv_full), kc & 1, lim, &abort_flag);
+                if (ok) ok = mbar_wait(smem_u32(&bars.q_full[g % kQStages]), (g / kQStages) & 1, lim, &abort_flag);
                 if (!ok) break;
                 tc_fence_after();
-                // dV += P^T dO_i
+                issue_s(g % kQStages);
+                issue_dp(g % kQStages);
+                for (int i = 0; i < I.n_it; ++i) {
+                    const int gi = g + i;
+                    const int s = gi % kQStages;
+                    const int s1 = (gi + 1) % kQStages;
+                    const bool more = i + 1 < I.n_it;
+                    const uint32_t sQ = sb + kOffQ + s * kTile, sDO = sb + kOffDO + s * kTile;
+                    // The loads of block i+1 (ready blocks ahead) are checked together with
+                    // P_i: every wait of an issuing thread can leave the tensor pipe idle.
+                    // P of an item's first block is computed after the P/dS warps have read
+                    // the previous item's dV and dK, so dV, dK may then be overwritten.
+                    ok = mbar_wait(smem_u32(&bars.p_full), gi & 1, lim, &abort_flag);
+                    if (ok && more)
+                        ok = mbar_wait(smem_u32(&bars.q_full[s1]), ((gi + 1) / kQStages) & 1, lim, &abort_flag);
+                    if (!ok) break;
+                    tc_fence_after();
+                    // dV += P^T dO_i
 #pragma unroll
-                for (int kk = 0; kk < kBlk / 16; ++kk)
-                    mma_bf16_ts(tmem + kColDV, tmem + kColS + 64 * (kk >> 2) + 8 * (kk & 3),
-                                sdesc_sw128(sDO + 2048 * kk, 16384, 1024), kIdescTS, (i > 0) || (kk > 0));
-                // next block's scores: the P/dS warps keep P_i in registers
-                if (more) issue_s(s1);
-                // one barrier per dS buffer: writing buffer i % 2 again needs block i's
-                // dK and dQ, so no waiter can fall two phases behind
-                ok = mbar_wait(smem_u32(&bars.ds_full[i & 1]), (i >> 1) & 1, lim, &abort_flag);
+                    for (int kk = 0; kk < kBlk / 16; ++kk)
+                        mma_bf16_ts(tmem + kColDV, tmem + kColS + 64 * (kk >> 2) + 8 * (kk & 3),
+                                    sdesc_sw128(sDO + 2048 * kk, 16384, 1024), kIdescTS, (i > 0) || (kk > 0));
+                    // next block's scores: the P/dS warps keep P_i in registers
+                    if (more) issue_s(s1);
+                    // one barrier per dS buffer: writing buffer gi % 2 again needs block gi's
+                    // dK and dQ, so no waiter can fall two phases behind
+                    ok = mbar_wait(smem_u32(&bars.ds_full[gi & 1]), (gi >> 1) & 1, lim, &abort_flag);
+                    if (!ok) break;
+                    tc_fence_after();
+                    // dK += dS^T Q_i
+#pragma unroll
+                    for (int kk = 0; kk < kBlk / 16; ++kk)
+                        mma_bf16_ts(tmem + kColDK, tmem + kColDP + 64 * (kk >> 2) + 8 * (kk & 3),
+                                    sdesc_sw128(sQ + 2048 * kk, 16384, 1024), kIdescTS, (i > 0) || (kk > 0));
+                    mma_commit(smem_u32(&bars.q_empty[s]));  // Q_i, dO_i, lse_i, delta_i consumed
+                    if (more) issue_dp(s1);
+                }
                 if (!ok) break;
-                tc_fence_after();
-                // dK += dS^T Q_i
-#pragma unroll
-                for (int kk = 0; kk < kBlk / 16; ++kk)
-                    mma_bf16_ts(tmem + kColDK, tmem + kColDP + 64 * (kk >> 2) + 8 * (kk & 3),
-                                sdesc_sw128(sQ + 2048 * kk, 16384, 1024), kIdescTS, (i > 0) || (kk > 0));
-                mma_commit(smem_u32(&bars.q_empty[s]));  // Q_i, dO_i, lse_i, delta_i consumed
-                if (more) issue_dp(s1);
+                mma_commit(smem_u32(&bars.all_done));  // the item's dV, dK are final
+                mma_commit(smem_u32(&bars.kv_empty));  // this thread's reads of K, V are done
+                g += I.n_it;
             }
-            if (ok) mma_commit(smem_u32(&bars.all_done));
             if (!ok) record_timeout(args.ctl, &abort_flag);
             mma_commit(smem_u32(&bars.drain));
             const volatile int never = 0;
@@ -318,26 +351,34 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         }
     } else if (C::kFusedDQ && warp == 2) {
         // ================================================================ dQ MMA issuer
-        // dQ_i = dS_i K_j (dS from its shared-memory buffer i % 2, K MN-major) into TMEM
-        // buffer i % 2.  A second issuing thread: its waits (dS_i, the dQ buffer) do not
+        // dQ_i = dS_i K_j (dS from its shared-memory buffer g % 2, K MN-major) into TMEM
+        // buffer g % 2.  A second issuing thread: its waits (dS_i, the dQ buffer) do not
         // stall the main MMA chain, and its MMAs read nothing that chain writes (dS in
         // shared memory, K) and write only the dQ buffers.
         if (lane == 0) {
             const uint32_t sK = sb + kOffK;
-            bool ok = mbar_wait(smem_u32(&bars.kv_full), 0, lim, &abort_flag);
-            for (int i = 0; i < n_it && ok; ++i) {
-                const int b = i & 1;
-                ok = mbar_wait(smem_u32(&bars.ds_full[b]), (i >> 1) & 1, lim, &abort_flag);
-                if (ok && i >= 2)
-                    ok = mbar_wait(smem_u32(&bars.dq_free[b]), ((i >> 1) & 1) ^ 1, lim, &abort_flag);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t sDS = sb + kOffDS + b * kDSBytes;
+            int g = 0, kc = 0;
+            bool ok = true;
+            for (int x = blockIdx.x; x < n_items && ok; x += gridDim.x, ++kc) {
+                const Item I = item_at(x);
+                ok = mbar_wait(smem_u32(&bars.kv_full), kc & 1, lim, &abort_flag);
+                for (int i = 0; i < I.n_it && ok; ++i) {
+                    const int gi = g + i, b = gi & 1;
+                    ok = mbar_wait(smem_u32(&bars.ds_full[b]), (gi >> 1) & 1, lim, &abort_flag);
+                    if (ok && gi >= 2)
+                        ok = mbar_wait(smem_u32(&bars.dq_free[b]), ((gi >> 1) & 1) ^ 1, lim, &abort_flag);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t sDS = sb + kOffDS + b * kDSBytes;
 #pragma unroll
-                for (int kk = 0; kk < kBlk / 16; ++kk)
-                    mma_bf16_ss(tmem + kColDQ + 64 * b, sdesc_sw128(sDS + 2048 * kk, 16384, 1024),
-                                sdesc_sw128(sK + 2048 * kk, 16384, 1024), kIdescDQ, kk > 0);
-                mma_commit(smem_u32(&bars.dq_full[b]));  // also: dS buffer b consumed
+                    for (int kk = 0; kk < kBlk / 16; ++kk)
+                        mma_bf16_ss(tmem + kColDQ + 64 * b, sdesc_sw128(sDS + 2048 * kk, 16384, 1024),
+                                    sdesc_sw128(sK + 2048 * kk, 16384, 1024), kIdescDQ, kk > 0);
+                    mma_commit(smem_u32(&bars.dq_full[b]));  // also: dS buffer b consumed
+                }
+                if (!ok) break;
+                mma_commit(smem_u32(&bars.kv_empty));  // this thread's reads of K are done
+                g += I.n_it;
             }
             if (!ok) record_timeout(args.ctl, &abort_flag);
             // drain this thread's MMAs before TMEM is released
@@ -354,98 +395,100 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         const uint32_t lb = tmem + (static_cast<uint32_t>(wq * 32) << 16);
         const float2 c2 = make_float2(args.c_log2, args.c_log2);
         bool ok = true;
-        for (int i = 0; i < n_it; ++i) {
-            const int s = i % kQStages;
-            // causal diagonal block: key k only reaches queries q >= k of the block
-            const bool diag = args.causal && (q_blk(i) == kvb);
-            ok = mbar_wait(smem_u32(&bars.q_full[s]), (i / kQStages) & 1, lim, &abort_flag);
-            if (ok) ok = mbar_wait(smem_u32(&bars.s_full), i & 1, lim, &abort_flag);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            tc_fence_after();
-            // -lse_i * log2(e) and -delta_i of this block's 64 queries
-            const float2* L2 = reinterpret_cast<const float2*>(sb_ptr + kOffL + s * kBlk * 4) + 32 * half;
-            const float2* D2 = reinterpret_cast<const float2*>(sb_ptr + kOffDelta + s * kBlk * 4) + 32 * half;
-            uint32_t pk[32];  // P^T row (64 queries) as bf16 pairs
-            {
-                uint32_t r[2][32];
-                tmem_ld32(lb + kColS + 64 * half, r[0]);
-                tmem_ld32(lb + kColS + 64 * half + 32, r[1]);
+        int g = 0, kc = 0;
+        for (int x = blockIdx.x; x < n_items && ok; x += gridDim.x, ++kc) {
+            const Item I = item_at(x);
+            for (int i = 0; i < I.n_it; ++i) {
+                const int gi = g + i;
+                const int s = gi % kQStages;
+                // causal diagonal block: key k only reaches queries q >= k of the block
+                const bool diag = args.causal && (q_blk(I, i) == I.kvb);
+                ok = mbar_wait(smem_u32(&bars.q_full[s]), (gi / kQStages) & 1, lim, &abort_flag);
+                if (ok) ok = mbar_wait(smem_u32(&bars.s_full), gi & 1, lim, &abort_flag);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
+                // -lse_i * log2(e) and -delta_i of this block's 64 queries
+                const float2* L2 = reinterpret_cast<const float2*>(sb_ptr + kOffL + s * kBlk * 4) + 32 * half;
+                const float2* D2 = reinterpret_cast<const float2*>(sb_ptr + kOffDelta + s * kBlk * 4) + 32 * half;
+                uint32_t pk[32];  // P^T row (64 queries) as bf16 pairs
+                {
+                    uint32_t r[2][32];
+                    tmem_ld32(lb + kColS + 64 * half, r[0]);
+                    tmem_ld32(lb + kColS + 64 * half + 32, r[1]);
 #pragma unroll
-                for (int x = 0; x < 32; ++x) {
-                    const uint32_t* rr = r[x / 16];
-                    const int e = 2 * (x % 16);
-                    float2 a = __ffma2_rn(make_float2(__uint_as_float(rr[e]), __uint_as_float(rr[e + 1])),
-                                          c2, L2[x]);
-                    if (diag) {
-                        const int q0 = 64 * half + 32 * (x / 16) + e;
-                        if (key_in_blk > q0) a.x = -INFINITY;
-                        if (key_in_blk > q0 + 1) a.y = -INFINITY;
+                    for (int x2 = 0; x2 < 32; ++x2) {
+                        const uint32_t* rr = r[x2 / 16];
+                        const int e = 2 * (x2 % 16);
+                        float2 a = __ffma2_rn(make_float2(__uint_as_float(rr[e]), __uint_as_float(rr[e + 1])),
+                                              c2, L2[x2]);
+                        if (diag) {
+                            const int q0 = 64 * half + 32 * (x2 / 16) + e;
+                            if (key_in_blk > q0) a.x = -INFINITY;
+                            if (key_in_blk > q0 + 1) a.y = -INFINITY;
+                        }
+                        pk[x2] = pack_bf16x2(ex2_approx(a.x), ex2_approx(a.y));
                     }
-                    pk[x] = pack_bf16x2(ex2_approx(a.x), ex2_approx(a.y));
                 }
-            }
-            // P^T of this half goes inside the columns this half read (the other half's
-            // scores may still be unread): queries 64h..64h+63 -> columns 64h..64h+31
-            tmem_st32(lb + kColS + 64 * half, pk);
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(smem_u32(&bars.p_full));
+                // P^T of this half goes inside the columns this half read (the other half's
+                // scores may still be unread): queries 64h..64h+63 -> columns 64h..64h+31
+                tmem_st32(lb + kColS + 64 * half, pk);
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(smem_u32(&bars.p_full));
 
-            // dS^T = P^T o (dP^T - delta)
-            const int b = i & 1;
-            ok = mbar_wait(smem_u32(&bars.dp_full), i & 1, lim, &abort_flag);
-            if (C::kFusedDQ && ok && i >= 2)
-                ok = mbar_wait(smem_u32(&bars.ds_empty[b]), ((i >> 1) & 1) ^ 1, lim, &abort_flag);
+                // dS^T = P^T o (dP^T - delta)
+                const int b = gi & 1;
+                ok = mbar_wait(smem_u32(&bars.dp_full), gi & 1, lim, &abort_flag);
+                if (C::kFusedDQ && ok && gi >= 2)
+                    ok = mbar_wait(smem_u32(&bars.ds_empty[b]), ((gi >> 1) & 1) ^ 1, lim, &abort_flag);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
+                uint8_t* dsrow = sb_ptr + kOffDS + b * kDSBytes + half * 16384 + key_in_blk * 128;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t r[32];
+                    tmem_ld32(lb + kColDP + 64 * half + 32 * h, r);
+                    uint32_t w[16];
+#pragma unroll
+                    for (int x2 = 0; x2 < 16; ++x2) {
+                        const uint32_t pp = pk[16 * h + x2];
+                        const float2 p = make_float2(__uint_as_float(pp << 16), __uint_as_float(pp & 0xFFFF0000u));
+                        const float2 gg = __fadd2_rn(make_float2(__uint_as_float(r[2 * x2]), __uint_as_float(r[2 * x2 + 1])),
+                                                     D2[16 * h + x2]);
+                        const float2 ds = __fmul2_rn(p, gg);
+                        w[x2] = pack_bf16x2(ds.x, ds.y);
+                    }
+                    tmem_st16(lb + kColDP + 64 * half + 16 * h, w);
+                    if constexpr (C::kFusedDQ) {
+                        // queries 64*half + 32h .. +31 of this key row -> MN-major swizzled A tile
+                        // for dQ: column `half`, row = key, 16-byte granule ((query % 64) / 8) ^ (key % 8)
+#pragma unroll
+                        for (int g4 = 0; g4 < 4; ++g4) {
+                            const int gran = (h * 4 + g4) ^ (key_in_blk & 7);
+                            *reinterpret_cast<uint4*>(dsrow + gran * 16) =
+                                make_uint4(w[4 * g4], w[4 * g4 + 1], w[4 * g4 + 2], w[4 * g4 + 3]);
+                        }
+                    }
+                }
+                tmem_st_wait();
+                if constexpr (C::kFusedDQ) fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(smem_u32(&bars.ds_full[gi & 1]));
+            }
+            if (!ok) break;
+            // epilogue: warps 4-7 store dV, warps 8-11 store dK (times scale).  Their TMEM
+            // reads finish before these warps compute the next item's first P.
+            ok = mbar_wait(smem_u32(&bars.all_done), kc & 1, lim, &abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            uint8_t* dsrow = sb_ptr + kOffDS + b * kDSBytes + half * 16384 + key_in_blk * 128;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t r[32];
-                tmem_ld32(lb + kColDP + 64 * half + 32 * h, r);
-                uint32_t w[16];
-#pragma unroll
-                for (int x = 0; x < 16; ++x) {
-                    const uint32_t pp = pk[16 * h + x];
-                    const float2 p = make_float2(__uint_as_float(pp << 16), __uint_as_float(pp & 0xFFFF0000u));
-                    const float2 g = __fadd2_rn(make_float2(__uint_as_float(r[2 * x]), __uint_as_float(r[2 * x + 1])),
-                                                D2[16 * h + x]);
-                    const float2 ds = __fmul2_rn(p, g);
-                    w[x] = pack_bf16x2(ds.x, ds.y);
-                }
-                tmem_st16(lb + kColDP + 64 * half + 16 * h, w);
-                if constexpr (C::kFusedDQ) {
-                    // queries 64*half + 32h .. +31 of this key row -> MN-major swizzled A tile
-                    // for dQ: column `half`, row = key, 16-byte granule ((query % 64) / 8) ^ (key % 8)
-#pragma unroll
-                    for (int g4 = 0; g4 < 4; ++g4) {
-                        const int gran = (h * 4 + g4) ^ (key_in_blk & 7);
-                        *reinterpret_cast<uint4*>(dsrow + gran * 16) =
-                            make_uint4(w[4 * g4], w[4 * g4 + 1], w[4 * g4 + 2], w[4 * g4 + 3]);
-                    }
-                }
-            }
-            tmem_st_wait();
-            if constexpr (C::kFusedDQ) fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(smem_u32(&bars.ds_full[i & 1]));
-        }
-        // epilogue: warps 4-7 store dV, warps 8-11 store dK (times scale)
-        if (ok) {
-            ok = mbar_wait(smem_u32(&bars.all_done), 0, lim, &abort_flag);
-            ok = __all_sync(0xffffffffu, ok);
-        }
-        if (!ok) {
-            if (lane == 0) record_timeout(args.ctl, &abort_flag);
-        } else {
-            tc_fence_after();
-            const int key = kvb * kBlk + key_in_blk;
+            const int key = I.kvb * kBlk + key_in_blk;
             const float sc = half ? args.scale : 1.0f;
             void* dst = half ? args.dk : args.dv;
             const uint32_t col = half ? kColDK : kColDV;
-            uint16_t* out = static_cast<uint16_t*>(dst) + (static_cast<size_t>(bh) * N + key) * kD;
+            uint16_t* out = static_cast<uint16_t*>(dst) + (static_cast<size_t>(I.bh) * N + key) * kD;
 #pragma unroll
             for (int h = 0; h < kD / 32; ++h) {
                 uint32_t r[32];
@@ -453,15 +496,17 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                 if (key < N) {
                     uint4* o4 = reinterpret_cast<uint4*>(out + 32 * h);
 #pragma unroll
-                    for (int x = 0; x < 4; ++x)
-                        o4[x] = make_uint4(
-                            pack_bf16x2(__uint_as_float(r[8 * x]) * sc, __uint_as_float(r[8 * x + 1]) * sc),
-                            pack_bf16x2(__uint_as_float(r[8 * x + 2]) * sc, __uint_as_float(r[8 * x + 3]) * sc),
-                            pack_bf16x2(__uint_as_float(r[8 * x + 4]) * sc, __uint_as_float(r[8 * x + 5]) * sc),
-                            pack_bf16x2(__uint_as_float(r[8 * x + 6]) * sc, __uint_as_float(r[8 * x + 7]) * sc));
+                    for (int x2 = 0; x2 < 4; ++x2)
+                        o4[x2] = make_uint4(
+                            pack_bf16x2(__uint_as_float(r[8 * x2]) * sc, __uint_as_float(r[8 * x2 + 1]) * sc),
+                            pack_bf16x2(__uint_as_float(r[8 * x2 + 2]) * sc, __uint_as_float(r[8 * x2 + 3]) * sc),
+                            pack_bf16x2(__uint_as_float(r[8 * x2 + 4]) * sc, __uint_as_float(r[8 * x2 + 5]) * sc),
+                            pack_bf16x2(__uint_as_float(r[8 * x2 + 6]) * sc, __uint_as_float(r[8 * x2 + 7]) * sc));
                 }
             }
+            g += I.n_it;
         }
+        if (!ok && lane == 0) record_timeout(args.ctl, &abort_flag);
     } else if (C::kFusedDQ && warp >= 12) {
         // ================================================================ dQ drain
         // dQ_i (fp32, TMEM) -> this warp's 32 rows staged in dS buffer b, which the dQ_i
@@ -471,42 +516,46 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         // c ^ (r % 8)), so the 32 lanes' row writes hit distinct banks.  Buffer b is
         // handed back to the P/dS warps (ds_empty[b]) once the reductions have read it.
         const int wq = warp % 4;
-        const int row_in_blk = wq * 32 + lane;
         const uint32_t lb = tmem + (static_cast<uint32_t>(wq * 32) << 16);
         bool ok = true;
-        for (int i = 0; i < n_it; ++i) {
-            const int b = i & 1;
-            ok = mbar_wait(smem_u32(&bars.dq_full[b]), (i >> 1) & 1, lim, &abort_flag);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            tc_fence_after();
-            uint32_t r[2][32];
-            tmem_ld32(lb + kColDQ + 64 * b, r[0]);
-            tmem_ld32(lb + kColDQ + 64 * b + 32, r[1]);
-            tc_fence_before();
-            mbar_arrive(smem_u32(&bars.dq_free[b]));
-            const uint32_t box0 = sb + kOffDS + b * kDSBytes + wq * 8192;  // two 4 KB boxes
+        int g = 0;
+        for (int x = blockIdx.x; x < n_items && ok; x += gridDim.x) {
+            const Item I = item_at(x);
+            for (int i = 0; i < I.n_it; ++i) {
+                const int gi = g + i, b = gi & 1;
+                ok = mbar_wait(smem_u32(&bars.dq_full[b]), (gi >> 1) & 1, lim, &abort_flag);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
+                uint32_t r[2][32];
+                tmem_ld32(lb + kColDQ + 64 * b, r[0]);
+                tmem_ld32(lb + kColDQ + 64 * b + 32, r[1]);
+                tc_fence_before();
+                mbar_arrive(smem_u32(&bars.dq_free[b]));
+                const uint32_t box0 = sb + kOffDS + b * kDSBytes + wq * 8192;  // two 4 KB boxes
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
+                for (int h = 0; h < 2; ++h)
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const uint32_t dst = box0 + h * 4096 + lane * 128 + ((c ^ (lane & 7)) << 4);
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst),
-                                 "r"(r[h][4 * c]), "r"(r[h][4 * c + 1]), "r"(r[h][4 * c + 2]),
-                                 "r"(r[h][4 * c + 3])
-                                 : "memory");
+                    for (int c = 0; c < 8; ++c) {
+                        const uint32_t dst = box0 + h * 4096 + lane * 128 + ((c ^ (lane & 7)) << 4);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst),
+                                     "r"(r[h][4 * c]), "r"(r[h][4 * c + 1]), "r"(r[h][4 * c + 2]),
+                                     "r"(r[h][4 * c + 3])
+                                     : "memory");
+                    }
+                fence_proxy_async_smem();  // generic-proxy writes -> visible to the TMA unit
+                __syncwarp();
+                if (lane == 0) {
+                    const int y = q_blk(I, i) * kBlk + wq * 32;
+                    tma_reduce_add_3d(&tm_dq, box0, 0, y, q_head(I, i));
+                    tma_reduce_add_3d(&tm_dq, box0 + 4096, 32, y, q_head(I, i));
+                    bulk_commit_group();
+                    bulk_wait_read_all();
+                    mbar_arrive(smem_u32(&bars.ds_empty[b]));
                 }
-            fence_proxy_async_smem();  // generic-proxy writes -> visible to the TMA unit
-            __syncwarp();
-            if (lane == 0) {
-                const int y = q_blk(i) * kBlk + wq * 32;
-                tma_reduce_add_3d(&tm_dq, box0, 0, y, q_head(i));
-                tma_reduce_add_3d(&tm_dq, box0 + 4096, 32, y, q_head(i));
-                bulk_commit_group();
-                bulk_wait_read_all();
-                mbar_arrive(smem_u32(&bars.ds_empty[b]));
+                __syncwarp();
             }
-            __syncwarp();
+            g += I.n_it;
         }
         // the reductions must complete before the CTA's shared memory goes away
         if (lane == 0) bulk_wait_all();
@@ -653,7 +702,10 @@ int launch_bwd_impl(const void* q, const void* k, const void* v, const void* o, 
     a.c_log2 = scale * kLog2e;
     a.scale = scale;
     a.ctl = ctl;
-    bwd_main_kernel<D><<<a.n_kv * BH_kv, C::kThreads, C::kSmemAlloc, s>>>(tq, tk, tv, tdo, tdq, a);
+    // persistent: one CTA per SM (fewer if there are fewer items), each looping over items
+    const int n_items = a.n_kv * BH_kv;
+    const int grid = n_items < sms ? n_items : sms;
+    bwd_main_kernel<D><<<grid, C::kThreads, C::kSmemAlloc, s>>>(tq, tk, tv, tdo, tdq, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return static_cast<int>(e);
 
