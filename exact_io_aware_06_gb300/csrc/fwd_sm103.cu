@@ -52,6 +52,8 @@ struct FwdArgs {
     int N_kv;         // keys per head (= N except for a key shard)
     int delta;        // causal: key j reaches query i iff j <= i + delta (0 unless sharded)
     int n_pairs;      // query-tile pairs per head
+    int BH;           // query heads (B * H)
+    int hgrp;         // causal: heads per scheduling group (see the tile mapping)
     float c_log2;     // scale * log2(e) (times the FP8 descales)
     float o_scale;    // multiplies O at the end (FP8: v descale), 1 otherwise
     int causal;
@@ -181,11 +183,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         (smem_u32(smem_raw) + 1023u) & ~1023u;  // 1 KB aligned for the 128 B swizzle
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
-    // ---- tile coordinates: within a head, heaviest (last) query pair first
-    const int bh = blockIdx.x / args.n_pairs;
+    // ---- tile coordinates.  Non-causal: head-major, every pair of a head together (the
+    // head's K/V stays in L2).  Causal: a pair's work grows with its index, so CTAs are
+    // issued heaviest pair first across a group of hgrp heads (whose K/V fits in L2),
+    // group after group; head-major order would start the last heads' heaviest pairs
+    // near the end of the grid and leave a long tail.
+    int bh, pair;
+    if (args.causal) {
+        const int span = args.hgrp * args.n_pairs;
+        const int grp = blockIdx.x / span;
+        const int hg = min(args.hgrp, args.BH - grp * args.hgrp);  // heads in this group
+        const int xi = blockIdx.x - grp * span;
+        pair = args.n_pairs - 1 - xi / hg;
+        bh = grp * args.hgrp + xi % hg;
+    } else {
+        bh = blockIdx.x / args.n_pairs;
+        pair = args.n_pairs - 1 - (blockIdx.x % args.n_pairs);
+    }
     // grouped-query attention: H / H_kv query heads share one K/V head
     const int bh_kv = (bh / args.H) * args.H_kv + (bh % args.H) / (args.H / args.H_kv);
-    const int pair = args.n_pairs - 1 - (blockIdx.x % args.n_pairs);
     const int r0 = pair * 2 * kBM;
     const int N = args.N;
     const int N_kv = SHARD ? args.N_kv : N;
@@ -549,6 +565,14 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse
     a.N_kv = N_kv;
     a.delta = delta;
     a.n_pairs = (N + 2 * kBM - 1) / (2 * kBM);
+    a.BH = BH;
+    {
+        // causal scheduling groups: as many heads as keep their K/V within ~64 MB of L2
+        // (K/V bytes per query head: a K/V head's K and V over the heads that share it)
+        const double kv_head = 2.0 * static_cast<double>(N_kv) * D * C::kElem / (H / H_kv);
+        long long g = static_cast<long long>(64.0 * 1024 * 1024 / (kv_head > 1.0 ? kv_head : 1.0));
+        a.hgrp = static_cast<int>(g < 1 ? 1 : (g > BH ? BH : g));
+    }
     a.c_log2 = c_log2;
     a.o_scale = o_scale;
     a.causal = causal;
