@@ -157,12 +157,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const int N = args.N, Np = args.Np;
     const int n_q = Np / kBlk;
     const int G = args.H / args.H_kv;
-    // Persistent: this CTA works through items x = blockIdx.x, + gridDim.x, ... where an
-    // item is one (K/V head bh, 128-key block kvb).  Causal items go heaviest first
-    // (kvb = 0 meets every query block).  Every role walks the same item sequence and
-    // numbers the query blocks g = 0, 1, 2, ... across items: stages and barrier
-    // phases follow g, the K/V tile and the dK/dV accumulators follow the item count.
+    // Persistent: an item is one (K/V head bh, 128-key block kvb); causal items are
+    // numbered heaviest first (kvb = 0 meets every query block).  This CTA takes item
+    // x = k * gridDim.x + c in round k, with c = blockIdx.x in even rounds and
+    // gridDim.x - 1 - blockIdx.x in odd ones: alternating the direction balances the
+    // heavy-first causal work across CTAs about as well as dynamic dispatch, and every
+    // role can compute the sequence on its own.  Every role numbers the query blocks
+    // g = 0, 1, 2, ... across items: stages and barrier phases follow g, the K/V tile
+    // and the dK/dV accumulators follow the item count.
     const int n_items = args.n_kv * args.BH;
+    auto item_x = [&](int k) {
+        const int c = (k & 1) ? static_cast<int>(gridDim.x - 1 - blockIdx.x) : static_cast<int>(blockIdx.x);
+        return k * static_cast<int>(gridDim.x) + c;
+    };
     struct Item {
         int bh, kvb, i0, n_loc, n_it;
     };
@@ -230,7 +237,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             const uint32_t kvf = smem_u32(&bars.kv_full);
             int g = 0, kc = 0;
             bool ok = true;
-            for (int x = blockIdx.x; x < n_items && ok; x += gridDim.x, ++kc) {
+            for (int k = 0, x = item_x(0); x < n_items && ok; x = item_x(++k), ++kc) {
                 const Item I = item_at(x);
                 // this item's K/V over the previous item's, once that one is consumed
                 if (kc > 0 && !mbar_wait(smem_u32(&bars.kv_empty), (kc - 1) & 1, lim, &abort_flag)) {
@@ -294,7 +301,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             };
             int g = 0, kc = 0;
             bool ok = true;
-            for (int x = blockIdx.x; x < n_items && ok; x += gridDim.x, ++kc) {
+            for (int k = 0, x = item_x(0); x < n_items && ok; x = item_x(++k), ++kc) {
                 const Item I = item_at(x);
                 // the item's first scores; S and dP of the previous item's last block were
                 // read by its dV and dK, issued before these by this thread
@@ -359,7 +366,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             const uint32_t sK = sb + kOffK;
             int g = 0, kc = 0;
             bool ok = true;
-            for (int x = blockIdx.x; x < n_items && ok; x += gridDim.x, ++kc) {
+            for (int k = 0, x = item_x(0); x < n_items && ok; x = item_x(++k), ++kc) {
                 const Item I = item_at(x);
                 ok = mbar_wait(smem_u32(&bars.kv_full), kc & 1, lim, &abort_flag);
                 for (int i = 0; i < I.n_it && ok; ++i) {
@@ -396,7 +403,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         const float2 c2 = make_float2(args.c_log2, args.c_log2);
         bool ok = true;
         int g = 0, kc = 0;
-        for (int x = blockIdx.x; x < n_items && ok; x += gridDim.x, ++kc) {
+        for (int k = 0, x = item_x(0); x < n_items && ok; x = item_x(++k), ++kc) {
             const Item I = item_at(x);
             for (int i = 0; i < I.n_it; ++i) {
                 const int gi = g + i;
@@ -519,7 +526,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         const uint32_t lb = tmem + (static_cast<uint32_t>(wq * 32) << 16);
         bool ok = true;
         int g = 0;
-        for (int x = blockIdx.x; x < n_items && ok; x += gridDim.x) {
+        for (int k = 0, x = item_x(0); x < n_items && ok; x = item_x(++k)) {
             const Item I = item_at(x);
             for (int i = 0; i < I.n_it; ++i) {
                 const int gi = g + i, b = gi & 1;
