@@ -45,6 +45,15 @@ constexpr int kStages = 2;       // K ring and V ring depth
 constexpr int kThreads = 384;    // 12 warps
 constexpr float kTau = 8.0f;     // lazy-rescale threshold, log2 units
 
+// Store a box from shared memory to global memory through the tensor map (TMA),
+// tracked by the thread's bulk async-group; rows past the tensor's end are not written.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
 struct FwdArgs {
     void* o;          // bf16 [BH][N][D], or float32 when o_f32
     float* lse;
@@ -95,6 +104,7 @@ struct Bars {
     uint64_t k_full[kStages], k_empty[kStages];
     uint64_t v_full[kStages], v_empty[kStages];
     uint64_t s_full[2], p_full[2], o_done[2];
+    uint64_t o_staged[2];  // a tile's O rows are in shared memory (bf16 outputs)
     uint64_t drain;
 };
 
@@ -172,7 +182,8 @@ __device__ __forceinline__ float block_extreme(const uint32_t (&r)[128], bool wa
 template <int D, bool FP8, bool SHARD>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_v, const FwdArgs args) {
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                     const FwdArgs args) {
     using C = Cfg<D, FP8>;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) Bars bars;
@@ -224,6 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&bars.s_full[t]), 1);
             mbar_init(smem_u32(&bars.p_full[t]), 128);
             mbar_init(smem_u32(&bars.o_done[t]), 1);
+            mbar_init(smem_u32(&bars.o_staged[t]), 128);
         }
         mbar_init(smem_u32(&bars.drain), 1);
         fence_barrier_init();
@@ -494,31 +506,71 @@ __global__ void __launch_bounds__(kThreads, 1)
             // lse = -inf: its O columns hold P V with P = 0, or were never written
             const float inv = (!SHARD || l > 0.f) ? o_scale / l : 0.f;
             const size_t orow = (static_cast<size_t>(bh) * N + qrow) * D;
+            if constexpr (!SHARD && !FP8) {
+                // Coalesced O: each row goes into this tile's Q buffer (free: every S MMA
+                // of the tile completed before o_done) in the 128-byte swizzled layout
+                // (16-byte granule g of row r at g ^ (r % 8)); one thread then writes the
+                // tile with TMA stores of whole lines.  Rows past N are clipped by the TMA.
+                const uint32_t stage = smem_base + C::kOffQ + t * C::kTileBytes;
 #pragma unroll
-            for (int q4 = 0; q4 < D / 32; ++q4) {
-                uint32_t ov[32];
-                if (!SHARD || n_kv > 0) {
+                for (int q4 = 0; q4 < D / 32; ++q4) {
+                    uint32_t ov[32];
                     tmem_ld32(lane_base + colO + 32 * q4, ov);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) ov[i] = 0u;
-                }
-                if (SHARD && qrow < N) {
-                    float4* out = reinterpret_cast<float4*>(static_cast<float*>(args.o) + orow + 32 * q4);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        out[i] = make_float4(__uint_as_float(ov[4 * i]) * inv, __uint_as_float(ov[4 * i + 1]) * inv,
-                                             __uint_as_float(ov[4 * i + 2]) * inv, __uint_as_float(ov[4 * i + 3]) * inv);
-                } else if (qrow < N) {
                     uint32_t w[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
-                        w[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv,
-                                           __uint_as_float(ov[2 * i + 1]) * inv);
-                    uint4* out = reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.o) + orow + 32 * q4);
+                        w[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv, __uint_as_float(ov[2 * i + 1]) * inv);
+                    const uint32_t rowbase = stage + (q4 >> 1) * C::kChunkBytes + row_in_tile * 128;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        out[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                    for (int i = 0; i < 4; ++i) {
+                        const int gran = ((q4 & 1) * 4 + i) ^ (row_in_tile & 7);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(rowbase + gran * 16),
+                                     "r"(w[4 * i]), "r"(w[4 * i + 1]), "r"(w[4 * i + 2]), "r"(w[4 * i + 3])
+                                     : "memory");
+                    }
+                }
+                fence_proxy_async_smem();  // generic-proxy writes -> visible to the TMA unit
+                mbar_arrive(smem_u32(&bars.o_staged[t]));
+                if (wq == 0 && lane == 0) {
+                    // bounded: a warp that gave up never arrives, and this wait then ends too
+                    if (mbar_wait(smem_u32(&bars.o_staged[t]), 0, lim, &abort_flag)) {
+#pragma unroll
+                        for (int c = 0; c < C::kChunks; ++c)
+                            tma_store_3d(&tm_o, stage + c * C::kChunkBytes, c * 64, r0 + t * kBM, bh);
+                        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                        // complete before the CTA exits (its shared memory is released)
+                        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+                    } else {
+                        record_timeout(args.ctl, &abort_flag);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int q4 = 0; q4 < D / 32; ++q4) {
+                    uint32_t ov[32];
+                    if (!SHARD || n_kv > 0) {
+                        tmem_ld32(lane_base + colO + 32 * q4, ov);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) ov[i] = 0u;
+                    }
+                    if (SHARD && qrow < N) {
+                        float4* out = reinterpret_cast<float4*>(static_cast<float*>(args.o) + orow + 32 * q4);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            out[i] = make_float4(__uint_as_float(ov[4 * i]) * inv, __uint_as_float(ov[4 * i + 1]) * inv,
+                                                 __uint_as_float(ov[4 * i + 2]) * inv, __uint_as_float(ov[4 * i + 3]) * inv);
+                    } else if (qrow < N) {
+                        uint32_t w[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            w[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv,
+                                               __uint_as_float(ov[2 * i + 1]) * inv);
+                        uint4* out = reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.o) + orow + 32 * q4);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            out[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                    }
                 }
             }
             if (qrow < N && args.lse != nullptr)
@@ -547,6 +599,10 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse
     int rc = make_map_3d(&tq, q, dt, C::kElem, D, N, BH, C::kBoxX, kBM);
     if (rc == 0) rc = make_map_3d(&tk, k, dt, C::kElem, D, N_kv, BH_kv, C::kBoxX, kBN);
     if (rc == 0) rc = make_map_3d(&tv, v, dt, C::kElem, D, N_kv, BH_kv, C::kBoxX, kBN);
+    // O [BH][N][D] bf16, written in (64 x 128) boxes (bf16 outputs only)
+    CUtensorMap to = tq;
+    if (rc == 0 && !SHARD && !FP8)
+        rc = make_map_3d(&to, o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, N, BH, 64, kBM);
     if (rc != 0) return rc;
     static uint64_t attr_set = 0;  // per template instance, one bit per device
     int dev = 0;
@@ -583,7 +639,7 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse
     a.v_descale = vd;
     a.ctl = ctl;
     dim3 grid(a.n_pairs * BH);
-    fwd_sm103_kernel<D, FP8, SHARD><<<grid, kThreads, C::kSmemAlloc, s>>>(tq, tk, tv, a);
+    fwd_sm103_kernel<D, FP8, SHARD><<<grid, kThreads, C::kSmemAlloc, s>>>(tq, tk, tv, to, a);
     return static_cast<int>(cudaGetLastError());
 }
 
