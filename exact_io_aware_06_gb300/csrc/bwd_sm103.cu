@@ -59,6 +59,14 @@ __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, uint32
         "r"(src), "r"(x), "r"(y), "r"(z)
         : "memory");
 }
+// Store a box from shared memory to global memory through the tensor map (TMA),
+// tracked by the thread's bulk async-group; rows past the tensor's end are not written.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -125,6 +133,7 @@ struct Bars {
     uint64_t ds_empty[2];
     uint64_t dq_full[2], dq_free[2];
     uint64_t all_done;
+    uint64_t epi_staged, epi_free;  // d = 64: an item's dV, dK staged / stored from smem
     uint64_t drain, drain2;
 };
 
@@ -137,7 +146,8 @@ template <int D>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                    const __grid_constant__ CUtensorMap tm_dq,
+                    const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dk,
+                    const __grid_constant__ CUtensorMap tm_dv,
                     const BwdArgs args) {
     using C = BwdCfg<D>;
     constexpr int kD = D, kQStages = C::kQStages, kTile = C::kTile, kChunks = C::kChunks;
@@ -211,6 +221,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         mbar_init(smem_u32(&bars.ds_full[0]), 256);
         mbar_init(smem_u32(&bars.ds_full[1]), 256);
         mbar_init(smem_u32(&bars.all_done), 1);
+        mbar_init(smem_u32(&bars.epi_staged), 256);
+        mbar_init(smem_u32(&bars.epi_free), 1);
         mbar_init(smem_u32(&bars.drain), 1);
         mbar_init(smem_u32(&bars.drain2), 1);
         fence_barrier_init();
@@ -220,7 +232,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
         tma_prefetch_desc(&tm_do);
-        if (C::kFusedDQ) tma_prefetch_desc(&tm_dq);
+        if (C::kFusedDQ) {
+            tma_prefetch_desc(&tm_dq);
+            tma_prefetch_desc(&tm_dk);
+            tma_prefetch_desc(&tm_dv);
+        }
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(&tmem_slot), kTmemCols);
@@ -449,6 +465,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                 ok = mbar_wait(smem_u32(&bars.dp_full), gi & 1, lim, &abort_flag);
                 if (C::kFusedDQ && ok && gi >= 2)
                     ok = mbar_wait(smem_u32(&bars.ds_empty[b]), ((gi >> 1) & 1) ^ 1, lim, &abort_flag);
+                // the previous item's dV, dK were staged in this buffer: their TMA stores
+                // must have read it
+                if (C::kFusedDQ && ok && i == 0 && kc > 0)
+                    ok = mbar_wait(smem_u32(&bars.epi_free), (kc - 1) & 1, lim, &abort_flag);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();
@@ -485,8 +505,55 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                 mbar_arrive(smem_u32(&bars.ds_full[gi & 1]));
             }
             if (!ok) break;
-            // epilogue: warps 4-7 store dV, warps 8-11 store dK (times scale).  Their TMEM
-            // reads finish before these warps compute the next item's first P.
+            if constexpr (C::kFusedDQ) {
+                // epilogue (d = 64): warps 4-7 stage dV, warps 8-11 dK (times scale) in the dS
+                // buffer that the next item's first block will use -- free once the drain has
+                // reduced the dQ staged there two blocks ago -- as 128-byte swizzled
+                // 128 x 64 boxes; one thread writes them with TMA stores of whole lines.
+                const int gn = g + I.n_it, bn = gn & 1;
+                ok = mbar_wait(smem_u32(&bars.all_done), kc & 1, lim, &abort_flag);
+                if (ok && gn >= 2)
+                    ok = mbar_wait(smem_u32(&bars.ds_empty[bn]), ((gn >> 1) & 1) ^ 1, lim, &abort_flag);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t box = sb + kOffDS + bn * kDSBytes + half * 16384;
+                const float sc = half ? args.scale : 1.0f;
+                const uint32_t col = half ? kColDK : kColDV;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t r[32];
+                    tmem_ld32(lb + col + 32 * h, r);
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        const int gran = (h * 4 + c4) ^ (key_in_blk & 7);
+                        const float* f = reinterpret_cast<const float*>(r) + 8 * c4;
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(box + key_in_blk * 128 + gran * 16),
+                                     "r"(pack_bf16x2(f[0] * sc, f[1] * sc)), "r"(pack_bf16x2(f[2] * sc, f[3] * sc)),
+                                     "r"(pack_bf16x2(f[4] * sc, f[5] * sc)), "r"(pack_bf16x2(f[6] * sc, f[7] * sc))
+                                     : "memory");
+                    }
+                }
+                fence_proxy_async_smem();  // generic-proxy writes -> visible to the TMA unit
+                mbar_arrive(smem_u32(&bars.epi_staged));
+                if (warp == 4 && lane == 0) {
+                    if (mbar_wait(smem_u32(&bars.epi_staged), kc & 1, lim, &abort_flag)) {
+                        tma_store_3d(&tm_dv, box - half * 16384, 0, I.kvb * kBlk, I.bh);
+                        tma_store_3d(&tm_dk, box - half * 16384 + 16384, 0, I.kvb * kBlk, I.bh);
+                        bulk_commit_group();
+                        bulk_wait_read_all();
+                        mbar_arrive(smem_u32(&bars.epi_free));
+                    } else {
+                        ok = false;
+                    }
+                }
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                g += I.n_it;
+                continue;
+            }
+            // epilogue (d = 128): warps 4-7 store dV, warps 8-11 store dK (times scale).
+            // Their TMEM reads finish before these warps compute the next item's first P.
             ok = mbar_wait(smem_u32(&bars.all_done), kc & 1, lim, &abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
@@ -513,6 +580,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             }
             g += I.n_it;
         }
+        // d = 64: the dV, dK stores complete before the CTA's shared memory goes away
+        if (C::kFusedDQ && warp == 4 && lane == 0) bulk_wait_all();
         if (!ok && lane == 0) record_timeout(args.ctl, &abort_flag);
     } else if (C::kFusedDQ && warp >= 12) {
         // ================================================================ dQ drain
@@ -682,9 +751,12 @@ int launch_bwd_impl(const void* q, const void* k, const void* v, const void* o, 
     if (rc == 0) rc = make_map_3d(&tv, v, dt, 2, D, N, BH_kv, 64, kBlk);
     if (rc == 0) rc = make_map_3d(&tdo, dO, dt, 2, D, N, BH, 64, kBlk);
     // fp32 accumulator [BH][Np][64], reduced into in 32 x 32 boxes (fused dQ only)
-    CUtensorMap tdq = tq;
+    CUtensorMap tdq = tq, tdk = tq, tdv = tq;
     if (rc == 0 && C::kFusedDQ)
         rc = make_map_3d(&tdq, dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, Np, BH, 32, 32);
+    // dK, dV [BH_kv][N][64] bf16, written in (64 x 128) boxes (fused d = 64 epilogue)
+    if (rc == 0 && C::kFusedDQ) rc = make_map_3d(&tdk, dk, dt, 2, D, N, BH_kv, 64, kBlk);
+    if (rc == 0 && C::kFusedDQ) rc = make_map_3d(&tdv, dv, dt, 2, D, N, BH_kv, 64, kBlk);
     if (rc != 0) return rc;
     static uint64_t attr_set = 0;
     if (dev >= 64 || !(attr_set & (1ull << dev))) {
@@ -712,7 +784,7 @@ int launch_bwd_impl(const void* q, const void* k, const void* v, const void* o, 
     // persistent: one CTA per SM (fewer if there are fewer items), each looping over items
     const int n_items = a.n_kv * BH_kv;
     const int grid = n_items < sms ? n_items : sms;
-    bwd_main_kernel<D><<<grid, C::kThreads, C::kSmemAlloc, s>>>(tq, tk, tv, tdo, tdq, a);
+    bwd_main_kernel<D><<<grid, C::kThreads, C::kSmemAlloc, s>>>(tq, tk, tv, tdo, tdq, tdk, tdv, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return static_cast<int>(e);
 
