@@ -18,7 +18,7 @@ on their own streams so that they overlap the other parts' compute.
 
 ``extras`` times the variant rows alone, after the step and outside ``value``
 (10 launches each after 3 warm-ups): backward at d=128 and causal, FP8 causal
-and per-head, grouped-query forward/backward (32 query heads on 8 K/V heads),
+and per-head and per-128-row-block scale factors, grouped-query forward/backward (32 query heads on 8 K/V heads),
 and the forward sharded over 4 key blocks of the sequence plus the lse merge
 (with the merge kernel's achieved HBM bandwidth).
 
@@ -274,6 +274,7 @@ EXTRAS = [
     ("bwd_bf16_b4h16n2048d64_causal", "bwd", 4, 16, 16, 2048, 64, True),
     ("fwd_e4m3_b4h16n4096d128_causal", "fwd8", 4, 16, 16, 4096, 128, True),
     ("fwd_e4m3_per_head_b4h16n4096d128", "fwd8h", 4, 16, 16, 4096, 128, False),
+    ("fwd_e4m3_per_block_b4h16n4096d128", "fwd8b", 4, 16, 16, 4096, 128, False),
     ("fwd_gqa_bf16_b1h32hkv8n16384d128_causal", "gqa_fwd", 1, 32, 8, 16384, 128, True),
     ("bwd_gqa_bf16_b1h32hkv8n16384d128_causal", "gqa_bwd", 1, 32, 8, 16384, 128, True),
     ("fwd_seq4shards_bf16_b1h32n16384d128_causal", "shard4", 1, 32, 32, 16384, 128, True),
@@ -288,6 +289,13 @@ def make_extra(torch, fa, inputs, ex, dev, stream):
     bf = lambda shape, seed: inputs.cast(inputs.normal(shape, seed), "bf16").to(dev)
     f_fwd = flops("fwd", B, H, N, d, causal)
     f_bwd = flops("fwdbwd", B, H, N, d, causal) - f_fwd
+    if what == "fwd8b":  # one E4M3 factor per 128-row block of each head
+        qb = [inputs.quantize_e4m3_per_block(inputs.normal((B, H, N, d), 42 + i)) for i in range(3)]
+        q8, k8, v8 = (c.to(dev) for c, _ in qb)
+        bd = [f.to(dev) for _, f in qb]
+        o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        return (lambda: fa.fa_fwd_fp8_per_block(q8, k8, v8, o, lse, *bd, s, causal, stream)), f_fwd, None
     if what in ("fwd8", "fwd8h"):
         x = inputs.attention_inputs(B, H, N, d, "e4m3")
         q8, k8, v8 = x["q"].to(dev), x["k"].to(dev), x["v"].to(dev)

@@ -15,7 +15,7 @@ import os
 
 __all__ = [
     "FaError", "FA_F32", "FA_BF16", "FA_E4M3", "lib", "fa_fwd", "fa_fwd_fp8", "fa_fwd_gqa",
-    "fa_fwd_fp8_per_head", "fa_bwd",
+    "fa_fwd_fp8_per_head", "fa_fwd_fp8_per_block", "fa_bwd",
     "fa_bwd_workspace_size", "fa_bwd_noalloc", "fa_last_device_error", "fa_set_wait_timeout_ns",
     "fa_selftest_wait_timeout", "fa_status_string", "attention_forward", "attention_backward",
 ]
@@ -52,6 +52,8 @@ def lib():
         L.fa_fwd_gqa.restype = i
         L.fa_fwd_fp8_per_head.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
         L.fa_fwd_fp8_per_head.restype = i
+        L.fa_fwd_fp8_per_block.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+        L.fa_fwd_fp8_per_block.restype = i
         ll = ctypes.c_longlong
         L.fa_fwd_kv_shard.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, ll, ll, i, vp]
         L.fa_fwd_kv_shard.restype = i
@@ -144,6 +146,21 @@ def fa_fwd_fp8_per_head(q8, k8, v8, o, lse, q_descale, k_descale, v_descale, sca
                                      _ptr(q_descale), _ptr(k_descale), _ptr(v_descale), B, H, N,
                                      d, float(scale), int(bool(causal)), _stream(stream)),
            "fa_fwd_fp8_per_head")
+
+
+def fa_fwd_fp8_per_block(q8, k8, v8, o, lse, q_descale, k_descale, v_descale, scale, causal,
+                         stream=None):
+    """FP8 forward with one descale per 128-row block of each head: float32 device
+    tensors of B*H*ceil(N/128) elements ([B][H][ceil(N/128)])."""
+    B, H, N, d = _shape(q8)
+    nb = (N + 127) // 128
+    for t in (q_descale, k_descale, v_descale):
+        if t.numel() != B * H * nb or t.dtype.itemsize != 4 or not t.is_contiguous():
+            raise ValueError("per-block descales: contiguous float32, B*H*ceil(N/128) elements")
+    _check(lib().fa_fwd_fp8_per_block(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(o), _ptr(lse),
+                                      _ptr(q_descale), _ptr(k_descale), _ptr(v_descale), B, H, N,
+                                      d, float(scale), int(bool(causal)), _stream(stream)),
+           "fa_fwd_fp8_per_block")
 
 
 def fa_fwd_kv_shard(q, k, v, o_part, lse_part, scale, causal, q_offset, kv_offset,

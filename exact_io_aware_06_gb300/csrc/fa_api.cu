@@ -116,7 +116,7 @@ __attribute__((visibility("default"))) int fa_fwd(const void* q, const void* k, 
     DevCtl ctl{st, g_wait_ns.load()};
     const float c_log2 = scale * 1.4426950408889634f;
     return from_cuda(
-        launch_fwd_sm103(q, k, v, o, lse, B, H, H, N, d, c_log2, 1.0f, nullptr, nullptr, nullptr,
+        launch_fwd_sm103(q, k, v, o, lse, B, H, H, N, d, c_log2, 1.0f, nullptr, nullptr, nullptr, 0,
                          causal ? 1 : 0, false, ctl, s));
 }
 
@@ -137,7 +137,7 @@ __attribute__((visibility("default"))) int fa_fwd_fp8(const void* q8, const void
     DevCtl ctl{st, g_wait_ns.load()};
     const float c_log2 = scale * q_descale * k_descale * 1.4426950408889634f;
     return from_cuda(launch_fwd_sm103(q8, k8, v8, o, lse, B, H, H, N, d, c_log2, v_descale, nullptr,
-                                      nullptr, nullptr, causal ? 1 : 0, true, ctl,
+                                      nullptr, nullptr, 0, causal ? 1 : 0, true, ctl,
                                       static_cast<cudaStream_t>(stream)));
 }
 
@@ -156,7 +156,7 @@ __attribute__((visibility("default"))) int fa_fwd_gqa(const void* q, const void*
     DevCtl ctl{st, g_wait_ns.load()};
     const float c_log2 = scale * 1.4426950408889634f;
     return from_cuda(launch_fwd_sm103(q, k, v, o, lse, B, H, H_kv, N, d, c_log2, 1.0f, nullptr,
-                                      nullptr, nullptr, causal ? 1 : 0, false, ctl,
+                                      nullptr, nullptr, 0, causal ? 1 : 0, false, ctl,
                                       static_cast<cudaStream_t>(stream)));
 }
 
@@ -176,7 +176,27 @@ __attribute__((visibility("default"))) int fa_fwd_fp8_per_head(
     DevCtl ctl{st, g_wait_ns.load()};
     const float c_log2 = scale * 1.4426950408889634f;
     return from_cuda(launch_fwd_sm103(q8, k8, v8, o, lse, B, H, H, N, d, c_log2, 1.0f, q_descale,
-                                      k_descale, v_descale, causal ? 1 : 0, true, ctl,
+                                      k_descale, v_descale, 0, causal ? 1 : 0, true, ctl,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+__attribute__((visibility("default"))) int fa_fwd_fp8_per_block(
+    const void* q8, const void* k8, const void* v8, void* o, float* lse, const float* q_descale,
+    const float* k_descale, const float* v_descale, int B, int H, int N, int d, float scale,
+    int causal, void* stream) {
+    int rc = check_common(q8, k8, v8, o, lse, B, H, N);
+    if (rc != FA_OK) return rc;
+    if (!std::isfinite(scale) || q_descale == nullptr || k_descale == nullptr ||
+        v_descale == nullptr)
+        return FA_ERR_INVALID_ARG;
+    if (d != 128) return FA_ERR_UNSUPPORTED;
+    int err = FA_OK;
+    int* st = status_word(&err);
+    if (st == nullptr) return err;
+    DevCtl ctl{st, g_wait_ns.load()};
+    const float c_log2 = scale * 1.4426950408889634f;
+    return from_cuda(launch_fwd_sm103(q8, k8, v8, o, lse, B, H, H, N, d, c_log2, 1.0f, q_descale,
+                                      k_descale, v_descale, 1, causal ? 1 : 0, true, ctl,
                                       static_cast<cudaStream_t>(stream)));
 }
 

@@ -69,7 +69,7 @@ struct FwdArgs {
     int H, H_kv;                 // query heads and K/V heads per batch (H % H_kv == 0)
     const float* qk_descale_q;   // optional per-(b, h) FP8 descales (device); null: none
     const float* qk_descale_k;   //   indexed by the tensor's own head (b*H + h / b*H_kv + g)
-    const float* v_descale;
+    const float* v_descale;      //   (per-block kernel: [head][ceil(rows / 128)])
     DevCtl ctl;
 };
 
@@ -179,7 +179,8 @@ __device__ __forceinline__ float block_extreme(const uint32_t (&r)[128], bool wa
 
 // SHARD: forward over a key shard (N_kv keys, causal offset delta, float32 O,
 // rows that see no key); compiled separately so the plain forward carries none of it.
-template <int D, bool FP8, bool SHARD>
+// PB (FP8 only): the descales are per 128-row block of each head instead of per head.
+template <int D, bool FP8, bool SHARD, bool PB = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -397,10 +398,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t colS = t ? C::kColS1 : C::kColS0;
         const uint32_t colO = t ? C::kColO1 : C::kColO0;
         // per-head FP8 descales fold into the score constant and the output scale
-        const float c = args.qk_descale_q
-                            ? args.c_log2 * args.qk_descale_q[bh] * args.qk_descale_k[bh_kv]
-                            : args.c_log2;
-        const float o_scale = args.v_descale ? args.v_descale[bh_kv] : args.o_scale;
+        float c = args.c_log2, o_scale = args.o_scale;
+        // per-block FP8 descales: this tile's Q factor folds into c, key block j's K factor
+        // into c_j = c * kd_j.  V's factor vd_j cannot be applied after P V has been
+        // accumulated, so it goes into P before the E4M3 rounding: P'_j = P_j vd_j / vd_max
+        // (at most P_j), by adding log2(vd_j / vd_max) <= 0 to the exponent; the row sum
+        // adds the block's sum times vd_max / vd_j, and O is scaled by vd_max at the end.
+        // The ratio is held at >= 2^-100, where P' is still exact in fp32, so that a zero
+        // factor keeps its block's mass in l.
+        const float* kd_blk = nullptr;
+        const float* vd_blk = nullptr;
+        float lg_vmax = 0.f;
+        if (PB) {
+            const int n_kb = (N_kv + kBN - 1) / kBN;
+            c *= args.qk_descale_q[static_cast<size_t>(bh) * ((N + kBM - 1) / kBM) + (r0 / kBM + t)];
+            kd_blk = args.qk_descale_k + static_cast<size_t>(bh_kv) * n_kb;
+            vd_blk = args.v_descale + static_cast<size_t>(bh_kv) * n_kb;
+            float vm = 0.f;
+            for (int x = lane; x < n_kb; x += 32) vm = fmaxf(vm, vd_blk[x]);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, off));
+            o_scale = vm;
+            lg_vmax = lg2_approx(vm);
+        } else if (args.qk_descale_q) {
+            c *= args.qk_descale_q[bh] * args.qk_descale_k[bh_kv];
+            o_scale = args.v_descale[bh_kv];
+        }
         const bool c_pos = c >= 0.f;
         // a masked score must become -inf after the multiply by c
         const uint32_t mask_bits = c_pos ? 0xff800000u : 0x7f800000u;
@@ -409,6 +432,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
 
         for (int j = 0; j < n_kv; ++j) {
+            // key block j's factors (per-block FP8), loaded before the wait
+            float cj = c, bj = 0.f, inv_rj = 1.f;
+            if (PB) {
+                const float kdj = __ldg(kd_blk + j), vdj = __ldg(vd_blk + j);
+                cj = c * kdj;
+                bj = fmaxf(lg2_approx(vdj) - lg_vmax, -100.f);
+                inv_rj = ex2_approx(-bj);
+            }
             ok = mbar_wait(smem_u32(&bars.s_full[t]), j & 1, lim, &abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
@@ -430,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (i >= valid) r[i] = mask_bits;
             }
             // block max of the scaled scores = c * (max of the raw scores) for c >= 0
-            const float mt = c * block_extreme(r, c_pos);
+            const float mt = cj * block_extreme(r, c_pos);
             // lazy rescale: move the reference only when the block max exceeds it by > kTau
             float alpha = 1.f;
             const bool bump = mt > m_ref + kTau;
@@ -440,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 l *= alpha;
             }
             const float ref = (m_ref == -INFINITY) ? 0.f : m_ref;
-            const float2 c2 = make_float2(c, c), nref2 = make_float2(-ref, -ref);
+            const float2 c2 = make_float2(cj, cj), nref2 = make_float2(bj - ref, bj - ref);
             float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0;
             if (FP8) {
                 uint32_t pk[32];
@@ -489,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             const float rs = (acc0.x + acc0.y) + (acc1.x + acc1.y);
-            l += rs;
+            l = (PB) ? fmaf(rs, inv_rj, l) : l + rs;
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(smem_u32(&bars.p_full[t]));
@@ -586,7 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D, bool FP8, bool SHARD>
+template <int D, bool FP8, bool SHARD, bool PB = false>
 int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                 int H_kv, int N, int N_kv, int delta, float c_log2, float o_scale,
                 const float* qd, const float* kd, const float* vd, int causal, DevCtl ctl,
@@ -608,7 +639,7 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 64 || !(attr_set & (1ull << dev))) {
-        cudaError_t e = cudaFuncSetAttribute(fwd_sm103_kernel<D, FP8, SHARD>,
+        cudaError_t e = cudaFuncSetAttribute(fwd_sm103_kernel<D, FP8, SHARD, PB>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::kSmemAlloc);
         if (e != cudaSuccess) return static_cast<int>(e);
@@ -639,7 +670,7 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse
     a.v_descale = vd;
     a.ctl = ctl;
     dim3 grid(a.n_pairs * BH);
-    fwd_sm103_kernel<D, FP8, SHARD><<<grid, kThreads, C::kSmemAlloc, s>>>(tq, tk, tv, to, a);
+    fwd_sm103_kernel<D, FP8, SHARD, PB><<<grid, kThreads, C::kSmemAlloc, s>>>(tq, tk, tv, to, a);
     return static_cast<int>(cudaGetLastError());
 }
 
@@ -647,8 +678,11 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse
 
 int launch_fwd_sm103(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                      int H, int H_kv, int N, int d, float c_log2, float o_scale, const float* qd,
-                     const float* kd, const float* vd, int causal, bool is_fp8, DevCtl ctl,
-                     cudaStream_t s) {
+                     const float* kd, const float* vd, int per_block, int causal, bool is_fp8,
+                     DevCtl ctl, cudaStream_t s) {
+    if (is_fp8 && per_block)
+        return launch_impl<128, true, false, true>(q, k, v, o, lse, B, H, H_kv, N, N, 0, c_log2,
+                                                   o_scale, qd, kd, vd, causal, ctl, s);
     if (is_fp8)
         return launch_impl<128, true, false>(q, k, v, o, lse, B, H, H_kv, N, N, 0, c_log2,
                                              o_scale, qd, kd, vd, causal, ctl, s);

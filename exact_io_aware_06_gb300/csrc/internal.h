@@ -27,12 +27,13 @@ cudaError_t launch_fwd_f32(const float* q, const float* k, const float* v, float
 
 // tcgen05 forward: bf16 (is_fp8 = false) or E4M3 inputs (is_fp8 = true, d = 128).
 // K/V have B*H_kv heads (H_kv = H: plain attention; H_kv < H: grouped-query).
-// qd/kd/vd: optional per-head FP8 descales on the device (null: use c_log2/o_scale only).
+// qd/kd/vd: optional per-head FP8 descales on the device (null: use c_log2/o_scale only);
+// with per_block = 1, one descale per 128-row block of each head ([head][ceil(N / 128)]).
 // Returns 0 on success, or a CUDA / tensor-map error code (non-zero).
 int launch_fwd_sm103(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                      int H, int H_kv, int N, int d, float c_log2, float o_scale, const float* qd,
-                     const float* kd, const float* vd, int causal, bool is_fp8, DevCtl ctl,
-                     cudaStream_t s);
+                     const float* kd, const float* vd, int per_block, int causal, bool is_fp8,
+                     DevCtl ctl, cudaStream_t s);
 
 // Forward over one shard of keys, bf16 inputs, d in {64, 128}: N_q queries against
 // N_kv keys; when causal, key j reaches query i iff j <= i + delta (delta = the

@@ -298,6 +298,11 @@ __device__ __forceinline__ float ex2_approx(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+__device__ __forceinline__ float lg2_approx(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 // two floats -> bf16x2 (round to nearest even); `lo` in bits 0-15.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

@@ -58,6 +58,21 @@ def quantize_e4m3_per_head(x):
     return codes, descale
 
 
+def quantize_e4m3_per_block(x, block=128):
+    """Per-(batch, head, 128-row block) amax quantisation of a [B, H, N, d] tensor.
+    Returns (uint8 codes, float32 descales of shape [B, H, ceil(N / block)])."""
+    B, H, N = x.shape[0], x.shape[1], x.shape[2]
+    nb = (N + block - 1) // block
+    codes = torch.empty(x.shape, dtype=torch.uint8)
+    descale = torch.empty((B, H, nb), dtype=torch.float32)
+    for b in range(B):
+        for h in range(H):
+            for j in range(nb):
+                rows = slice(j * block, min(N, (j + 1) * block))
+                codes[b, h, rows], descale[b, h, j] = quantize_e4m3(x[b, h, rows])
+    return codes, descale
+
+
 def attention_inputs(B, H, N, d, dtype="bf16", with_do=False,
                      seeds=(SEED_Q, SEED_K, SEED_V, SEED_DO)):
     """CPU tensors [B, H, N, d] for q, k, v (and do).  For ``e4m3`` the dict

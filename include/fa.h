@@ -122,6 +122,27 @@ int fa_fwd_fp8_per_head(const void* q8, const void* k8, const void* v8, void* o,
                         int B, int H, int N, int d, float scale, int causal, void* stream);
 
 /*
+ * FP8 forward with one dequantisation factor per 128-row block of each head, the
+ * finest scale granularity here ("Flash Attention V1/V2/V3演进", section V3增强:
+ * fine-grained scale factors).  Row i of head (b, h) of Q has the real value
+ * e4m3(q8[b][h][i]) * q_descale[(b*H + h) * nb + i / 128], nb = ceil(N / 128), and the
+ * same for K and V with their own arrays.  The result is the attention of the real
+ * values, as fa_fwd_fp8.
+ *
+ *   q_descale, k_descale, v_descale : DEVICE float32 arrays of B*H*ceil(N/128)
+ *                                     factors, positive and finite (read on the
+ *                                     device, not validated).
+ *   Other arguments as fa_fwd_fp8.
+ * Method: the Q and K factors fold into the score constant per (query tile, key
+ * block); V's factor for key block j scales P before its E4M3 rounding by
+ * v_j / max_j v_j (at most 1), and the row sum and O are corrected exactly.
+ * Errors: as fa_fwd_fp8_per_head.
+ */
+int fa_fwd_fp8_per_block(const void* q8, const void* k8, const void* v8, void* o, float* lse,
+                         const float* q_descale, const float* k_descale, const float* v_descale,
+                         int B, int H, int N, int d, float scale, int causal, void* stream);
+
+/*
  * Forward over one shard of the keys, the per-shard step of sequence-sharded
  * attention: N_q queries at global positions q_offset + i against N_kv keys at
  * global positions kv_offset + j.  It is the forward of "FlashAttention-1",

@@ -29,6 +29,10 @@ Functions (numpy in, numpy out; every array is promoted to float64):
   lse = -inf; ``lse_merge(o_parts, lse_parts)`` -- the two-state combination
   of "FlashAttention-1" 10.2.2 applied to normalised partial outputs.
 * ``e4m3_decode(codes, descale)`` / ``e4m3_encode(x)`` -- OCP FP8 E4M3.
+* ``e4m3_decode_blocks(codes, descales, block)`` -- E4M3 with one dequantisation
+  factor per block of rows (the finer scale factors of the "Flash Attention
+  V1/V2/V3" page, V3 section); the attention of the decoded values is
+  ``attn_fwd``.
 
 Tensors are ``[..., N, d]``; leading dimensions are flattened into heads.
 """
@@ -226,6 +230,18 @@ def e4m3_decode(codes, descale=1.0):
     out = np.empty(c.shape, dtype=np.float64)
     lib().oracle_e4m3_decode(_ptr(c, _u8p), c.size, float(descale), _ptr(out))
     return out
+
+
+def e4m3_decode_blocks(codes, descales, block=128):
+    """uint8 E4M3 codes [..., N, d] -> float64 values in which row i carries the
+    factor descales[..., i // block] (one per block of rows; the last block may be
+    short).  descales has shape [..., ceil(N / block)]."""
+    x = e4m3_decode(codes)
+    f = np.asarray(descales, dtype=np.float64)
+    N = x.shape[-2]
+    if f.shape != x.shape[:-2] + (-(-N // block),):
+        raise ValueError("descales: [..., ceil(N / block)] for codes [..., N, d]")
+    return x * f[..., np.arange(N) // block][..., None]
 
 
 def e4m3_encode(x):

@@ -98,6 +98,20 @@ def test_fp8_argument_errors(L):
     assert f(d=64) == 2
 
 
+@pytest.mark.parametrize("name", ["fa_fwd_fp8_per_head", "fa_fwd_fp8_per_block"])
+def test_fp8_descale_array_argument_errors(L, name):
+    fn = getattr(L, name)
+
+    def f(qd=P, kd=P, vd=P, d=128, N=128, scale=0.1):
+        return fn(P, P, P, P, None, qd, kd, vd, 1, 1, N, d, scale, 0, None)
+    assert f(qd=None) == 1
+    assert f(kd=None) == 1
+    assert f(vd=None) == 1
+    assert f(N=0) == 1
+    assert f(scale=float("nan")) == 1
+    assert f(d=64) == 2
+
+
 def test_bwd_argument_errors(L):
     ws = fa.fa_bwd_workspace_size(1, 1, 128, 64)
 

@@ -119,3 +119,98 @@ def test_fp8_per_head_b4_h16_n4096_d128_sampled():
         o_ref, _ = oracle.attn_fwd_rows(qh, kh, vh, rows, scale_for(d))
         vmax = np.abs(vh).max()
         assert max_err(o[b, h, rows], o_ref) <= fp8_o_bound(vmax)
+
+
+# ---------------------------------------------------------------- per-block FP8 factors
+def fp8_per_block(B, H, N, d, seed=0):
+    """Every 128-row block of every head gets its own range (0.1x to 10x), so a
+    per-tensor or per-head factor would waste bits; quantised per block."""
+    raw = {n: inputs.normal((B, H, N, d), 52 + i + seed) for i, n in enumerate("qkv")}
+    nb = (N + 127) // 128
+    g = torch.Generator().manual_seed(90 + seed)
+    out = {}
+    for n, x in raw.items():
+        spread = torch.logspace(-1, 1, nb)[torch.randperm(nb, generator=g)]
+        rows = spread.repeat_interleave(128)[:N].view(1, 1, N, 1)
+        out[n], out[n + "_descale"] = inputs.quantize_e4m3_per_block(x * rows)
+    return out
+
+
+def run_fp8_per_block(x, causal):
+    q = x["q"].cuda()
+    B, H, N, d = q.shape
+    o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    fa.fa_fwd_fp8_per_block(q, x["k"].cuda(), x["v"].cuda(), o, lse, x["q_descale"].cuda(),
+                            x["k_descale"].cuda(), x["v_descale"].cuda(), scale_for(d), causal)
+    check_status()
+    return f64(o), f64(lse)
+
+
+def per_block_bound(qh, kh, v8, vd, rows, scale, causal):
+    """Per-row bound on |O - O_ref| for the per-block kernel, from its arithmetic.
+    O = vd_max sum_j e4m3(P_j r_j) V8_j / l with r_j = vd_blk(j) / vd_max <= 1, against
+    the exact vd_max sum_j P_j r_j V8_j / l.  E4M3 rounding of x costs at most
+    2^-4 |x| for a normal x and 2^-10 for |x| < 2^-6 (subnormal spacing 2^-9); the
+    first part sums to at most 2^-4 max|V|.  The kernel's P is the one relative to
+    the row max times a factor >= 1 that divides out with l, so counting the keys
+    whose P_j r_j (taken relative to the row max) is below 2^-6 over-counts the
+    subnormal ones.  Adds the bf16 rounding of O (2^-8 max|V|) and 2^-12 max|V| for
+    the fp32 exponentials and sums."""
+    N = kh.shape[0]
+    S = scale * qh[rows] @ kh.T
+    if causal:
+        S = np.where(np.arange(N)[None, :] > np.asarray(rows)[:, None], -np.inf, S)
+    P = np.exp(S - S.max(axis=1, keepdims=True))
+    l = P.sum(axis=1)
+    r = (vd / vd.max())[np.arange(N) // 128]
+    v8max = np.abs(v8).max(axis=1)  # per key: max |E4M3 value|
+    sub = (P * r[None, :] < 2.0 ** -6) & (P > 0)
+    vmax = np.abs(v8 * vd[np.arange(N) // 128][:, None]).max()
+    return (2.0 ** -4 + 2.0 ** -8 + 2.0 ** -12) * vmax + 2.0 ** -10 * vd.max() * (sub * v8max[None, :]).sum(axis=1) / l
+
+
+def check_per_block_head(x, o, lse, b, h, rows, causal, d):
+    qh, kh, vh = (oracle.e4m3_decode_blocks(x[n][b, h].numpy(), x[n + "_descale"][b, h].numpy())
+                  for n in "qkv")
+    o_ref, lse_ref = oracle.attn_fwd_rows(qh, kh, vh, rows, scale_for(d), causal)
+    bound = per_block_bound(qh, kh, oracle.e4m3_decode(x["v"][b, h].numpy()),
+                            x["v_descale"][b, h].numpy().astype(np.float64), rows, scale_for(d), causal)
+    err = np.abs(o[b, h, rows] - o_ref).max(axis=1)
+    assert np.all(err <= bound), (err - bound).max()
+    assert max_err(lse[b, h, rows], lse_ref) <= TOL_LSE_FP8
+
+
+@pytest.mark.parametrize("N", [100, 300, 512])
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_per_block_small(N, causal):
+    B, H, d = 2, 3, 128
+    x = fp8_per_block(B, H, N, d)
+    o, lse = run_fp8_per_block(x, causal)
+    assert np.isfinite(o).all()
+    for b in range(B):
+        for h in range(H):
+            check_per_block_head(x, o, lse, b, h, np.arange(N), causal, d)
+
+
+def test_fp8_per_block_zero_v_block_keeps_its_mass():
+    # a V block quantised with factor 0 (all-zero values) still counts in the row sum:
+    # its keys take softmax mass and contribute nothing to O
+    B, H, N, d = 1, 2, 384, 128
+    x = fp8_per_block(B, H, N, d, seed=3)
+    x["v"][:, :, 128:256] = 0
+    x["v_descale"][:, :, 1] = 0.0
+    o, lse = run_fp8_per_block(x, False)
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    for h in range(H):
+        check_per_block_head(x, o, lse, 0, h, np.arange(N), False, d)
+
+
+def test_fp8_per_block_b4_h16_n4096_d128_sampled():
+    B, H, N, d = 4, 16, 4096, 128
+    x = fp8_per_block(B, H, N, d, seed=1)
+    for causal in (False, True):
+        o, lse = run_fp8_per_block(x, causal)
+        assert np.isfinite(o).all()
+        for b, h in ((0, 0), (2, 7), (3, 15)):
+            check_per_block_head(x, o, lse, b, h, sample_rows(N, 24, seed=b * 16 + h), causal, d)

@@ -491,3 +491,43 @@ def test_lse_merge_closed_forms():
     o, lse = oracle.lse_merge(np.stack([o_a, o_b]), np.stack([np.full(5, 800.0), np.full(5, -800.0)]))
     np.testing.assert_allclose(o, o_a, rtol=0, atol=1e-15)
     np.testing.assert_allclose(lse, 800.0, rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- per-block E4M3 factors
+def test_e4m3_decode_blocks_constant_factor_is_per_tensor_decode():
+    # one factor for every block is the per-tensor dequantisation
+    codes = np.random.default_rng(7).integers(0, 256, size=(2, 3, 300, 8), dtype=np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0  # drop the NaN codes
+    got = oracle.e4m3_decode_blocks(codes, np.full((2, 3, 3), 0.375))
+    np.testing.assert_array_equal(got, oracle.e4m3_decode(codes, 0.375))
+
+
+def test_e4m3_decode_blocks_factor_reaches_exactly_its_rows():
+    # Doubling an E4M3 value of magnitude <= 224 is exact.  Doubling the codes of rows
+    # 128..255 and halving block 1's factor must give identical values, and doubling
+    # the factor of block 2 (rows 256..299, a short block) must double only those rows.
+    rng = np.random.default_rng(8)
+    vals = rng.uniform(-200.0, 200.0, size=(300, 16))
+    codes = oracle.e4m3_encode(vals)
+    f = np.array([0.5, 0.25, 2.0])
+    base = oracle.e4m3_decode_blocks(codes, f)
+    codes2 = codes.copy()
+    codes2[128:256] = oracle.e4m3_encode(2.0 * oracle.e4m3_decode(codes[128:256]))
+    f2 = f.copy()
+    f2[1] /= 2
+    np.testing.assert_array_equal(oracle.e4m3_decode_blocks(codes2, f2), base)
+    f3 = f.copy()
+    f3[2] *= 2
+    got = oracle.e4m3_decode_blocks(codes, f3)
+    np.testing.assert_array_equal(got[:256], base[:256])
+    np.testing.assert_array_equal(got[256:], 2.0 * base[256:])
+    # row i has factor f[i // 128]
+    dec = oracle.e4m3_decode(codes)
+    for i in (0, 127, 128, 255, 256, 299):
+        np.testing.assert_array_equal(base[i], dec[i] * f[i // 128])
+
+
+def test_e4m3_decode_blocks_rejects_wrong_block_count():
+    codes = np.zeros((300, 4), dtype=np.uint8)
+    with pytest.raises(ValueError):
+        oracle.e4m3_decode_blocks(codes, np.ones(2))
