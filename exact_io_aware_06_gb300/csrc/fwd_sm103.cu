@@ -145,6 +145,37 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
     asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
     return d;
 }
+__device__ __forceinline__ float min3f(float a, float b, float c) {
+    float d;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Max (or, for a negative score scale, min) of the 128 raw scores: four
+// independent 3-input chains over r[4..123], then r[124..127].
+__device__ __forceinline__ float block_extreme(const uint32_t (&r)[128], bool want_max) {
+    float a[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) a[k] = __uint_as_float(r[k]);
+    if (want_max) {
+#pragma unroll
+        for (int i = 4; i < 124; i += 8)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                a[k] = max3f(a[k], __uint_as_float(r[i + 2 * k]), __uint_as_float(r[i + 2 * k + 1]));
+        a[0] = max3f(a[0], __uint_as_float(r[124]), __uint_as_float(r[125]));
+        a[1] = max3f(a[1], __uint_as_float(r[126]), __uint_as_float(r[127]));
+        return max3f(a[0], a[1], fmaxf(a[2], a[3]));
+    }
+#pragma unroll
+    for (int i = 4; i < 124; i += 8)
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            a[k] = min3f(a[k], __uint_as_float(r[i + 2 * k]), __uint_as_float(r[i + 2 * k + 1]));
+    a[0] = min3f(a[0], __uint_as_float(r[124]), __uint_as_float(r[125]));
+    a[1] = min3f(a[1], __uint_as_float(r[126]), __uint_as_float(r[127]));
+    return min3f(a[0], a[1], fminf(a[2], a[3]));
+}
 
 // SHARD: forward over a key shard (N_kv keys, causal offset delta, float32 O,
 // rows that see no key); compiled separately so the plain forward carries none of it.
@@ -429,65 +460,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < 128; ++i)
                     if (i >= valid) r[i] = mask_bits;
             }
-            // P_t(j) = exp2(c_j s - ref) with the reference as it stands, and the block
-            // max taken in the same pass from the exponent arguments: a block that does not
-            // move the reference (nearly every block after a row's first) is done in one
-            // pass, with the max off the exponentials' critical path.  Returns the row sum
-            // of this pass's P and stores P over the scores.
-            auto p_pass = [&](float ref, float& mx) -> float {
-                const float2 c2 = make_float2(cj, cj), nref2 = make_float2(bj - ref, bj - ref);
-                float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0;
-                float m0 = -INFINITY, m1 = -INFINITY;
-                if (FP8) {
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const float2 x01 = __ffma2_rn(
-                            make_float2(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1])), c2, nref2);
-                        const float2 x23 = __ffma2_rn(
-                            make_float2(__uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])), c2, nref2);
-                        m0 = max3f(m0, x01.x, x01.y);
-                        m1 = max3f(m1, x23.x, x23.y);
-                        const float2 p01 = make_float2(ex2_approx(x01.x), ex2_approx(x01.y));
-                        const float2 p23 = make_float2(ex2_approx(x23.x), ex2_approx(x23.y));
-                        acc0 = __fadd2_rn(acc0, p01);
-                        acc1 = __fadd2_rn(acc1, p23);
-                        pk[i] = pack_e4m3x4(p01.x, p01.y, p23.x, p23.y);
-                    }
-                    tmem_st32(lane_base + colS, pk);
-                } else {
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        uint32_t pk[32];
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const int e = 64 * h + 2 * i;
-                            const float2 x = __ffma2_rn(
-                                make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), c2, nref2);
-                            const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-                            if (i & 1) {
-                                m1 = max3f(m1, x.x, x.y);
-                                acc1 = __fadd2_rn(acc1, p);
-                            } else {
-                                m0 = max3f(m0, x.x, x.y);
-                                acc0 = __fadd2_rn(acc0, p);
-                            }
-                            pk[i] = pack_bf16x2(p.x, p.y);
-                        }
-                        tmem_st32(lane_base + colS + 32 * h, pk);
-                    }
-                }
-                mx = fmaxf(m0, m1);
-                return (acc0.x + acc0.y) + (acc1.x + acc1.y);
-            };
-            float mx;
-            float ref = (m_ref == -INFINITY) ? 0.f : m_ref;
-            float rs = p_pass(ref, mx);
-            // the block max of the scaled scores c_j s (masked scores are -inf)
-            const float mt = mx + ref - bj;
+            // block max of the scaled scores = c * (max of the raw scores) for c >= 0
+            const float mt = cj * block_extreme(r, c_pos);
             // lazy rescale: move the reference only when the block max exceeds it by > kTau
-            // (then P is recomputed; the pass stores P with warp-collective TMEM stores, so
-            // the whole warp repeats it, rows whose reference stayed rewriting the same P)
             float alpha = 1.f;
             const bool bump = mt > m_ref + kTau;
             if (bump) {
@@ -495,10 +470,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_ref = mt;
                 l *= alpha;
             }
-            if (__any_sync(0xffffffffu, bump)) {
-                tmem_st_wait();  // the first pass's stores land before the second's
-                ref = (m_ref == -INFINITY) ? 0.f : m_ref;
-                rs = p_pass(ref, mx);
+            const float ref = (m_ref == -INFINITY) ? 0.f : m_ref;
+            const float2 c2 = make_float2(cj, cj), nref2 = make_float2(bj - ref, bj - ref);
+            float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0;
+            if (FP8) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float2 x01 = __ffma2_rn(
+                        make_float2(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1])), c2, nref2);
+                    const float2 x23 = __ffma2_rn(
+                        make_float2(__uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])), c2, nref2);
+                    const float2 p01 = make_float2(ex2_approx(x01.x), ex2_approx(x01.y));
+                    const float2 p23 = make_float2(ex2_approx(x23.x), ex2_approx(x23.y));
+                    acc0 = __fadd2_rn(acc0, p01);
+                    acc1 = __fadd2_rn(acc1, p23);
+                    pk[i] = pack_e4m3x4(p01.x, p01.y, p23.x, p23.y);
+                }
+                tmem_st32(lane_base + colS, pk);
+            } else {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int e = 64 * h + 2 * i;
+                        const float2 x = __ffma2_rn(
+                            make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), c2, nref2);
+                        const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                        if (i & 1)
+                            acc1 = __fadd2_rn(acc1, p);
+                        else
+                            acc0 = __fadd2_rn(acc0, p);
+                        pk[i] = pack_bf16x2(p.x, p.y);
+                    }
+                    tmem_st32(lane_base + colS + 32 * h, pk);
+                }
             }
             if (j > 0 && __any_sync(0xffffffffu, bump)) {
                 // O_t += P V of the previous block has completed (it precedes S_t(j) in
@@ -512,6 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_st32(lane_base + colO + 32 * q4, ov);
                 }
             }
+            const float rs = (acc0.x + acc0.y) + (acc1.x + acc1.y);
             l = (PB) ? fmaf(rs, inv_rj, l) : l + rs;
             tmem_st_wait();
             tc_fence_before();
