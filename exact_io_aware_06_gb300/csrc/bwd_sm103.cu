@@ -246,6 +246,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
+    // launched while the delta pass may still run: its rows and the zeroed accumulator
+    // are read only after it has completed; the pass after this one may start launching
+    griddep_wait();
+    griddep_launch_dependents();
 
     if (warp == 0) {
         // ================================================================ producer
@@ -656,6 +660,7 @@ __global__ void bwd_prep_kernel(const uint4* __restrict__ o, const uint4* __rest
                                 const float* __restrict__ lse, float* __restrict__ ws_delta,
                                 float* __restrict__ ws_lse2, float4* __restrict__ dq_acc, int BH,
                                 int N, int Np, size_t acc_vec4) {
+    griddep_launch_dependents();  // the main kernel may launch and set up meanwhile
     const size_t tid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const size_t nthreads = static_cast<size_t>(gridDim.x) * blockDim.x;
     const size_t rows = static_cast<size_t>(BH) * Np;
@@ -691,6 +696,7 @@ __global__ void bwd_prep_kernel(const uint4* __restrict__ o, const uint4* __rest
 // dQ = bf16(scale * accumulator) for rows < N (d = 64); 8 elements per thread.
 __global__ void bwd_dq_convert_kernel(const float4* __restrict__ acc, uint4* __restrict__ dq,
                                       int N, int Np, size_t n_vec8, float scale) {
+    griddep_wait();  // launched while the main kernel may still run
     const size_t tid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const size_t nthreads = static_cast<size_t>(gridDim.x) * blockDim.x;
     constexpr int kVecPerRow = 64 / 8;
@@ -703,6 +709,25 @@ __global__ void bwd_dq_convert_kernel(const float4* __restrict__ acc, uint4* __r
         dq[x] = make_uint4(pack_bf16x2(a.x * scale, a.y * scale), pack_bf16x2(a.z * scale, a.w * scale),
                            pack_bf16x2(b.x * scale, b.y * scale), pack_bf16x2(b.z * scale, b.w * scale));
     }
+}
+
+// Launch with programmatic stream serialization: the kernel may start while the
+// previous kernel in the stream finishes; it calls griddep_wait() before reading
+// that kernel's results.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
 int grid_for(size_t work, int threads, int max_blocks) {
@@ -784,15 +809,15 @@ int launch_bwd_impl(const void* q, const void* k, const void* v, const void* o, 
     // persistent: one CTA per SM (fewer if there are fewer items), each looping over items
     const int n_items = a.n_kv * BH_kv;
     const int grid = n_items < sms ? n_items : sms;
-    bwd_main_kernel<D><<<grid, C::kThreads, C::kSmemAlloc, s>>>(tq, tk, tv, tdo, tdq, tdk, tdv, a);
-    e = cudaGetLastError();
+    e = launch_pdl(bwd_main_kernel<D>, dim3(grid), dim3(C::kThreads), C::kSmemAlloc, s, tq, tk, tv,
+                   tdo, tdq, tdk, tdv, a);
     if (e != cudaSuccess) return static_cast<int>(e);
 
     if constexpr (C::kFusedDQ) {
         const size_t n_vec8 = static_cast<size_t>(BH) * N * D / 8;
-        bwd_dq_convert_kernel<<<grid_for(n_vec8, 256, sms * 8), 256, 0, s>>>(
-            reinterpret_cast<const float4*>(dq_acc), static_cast<uint4*>(dq), N, Np, n_vec8, scale);
-        return static_cast<int>(cudaGetLastError());
+        return static_cast<int>(launch_pdl(bwd_dq_convert_kernel, dim3(grid_for(n_vec8, 256, sms * 8)),
+                                           dim3(256), 0, s, reinterpret_cast<const float4*>(dq_acc),
+                                           static_cast<uint4*>(dq), N, Np, n_vec8, scale));
     } else {
         // dQ by its own query-parallel kernel: recompute S and dP per query block
         return launch_bwd_dq(q, k, v, dO, ws_lse2, ws_delta, dq, B, H, H_kv, N, D, scale, causal,

@@ -293,6 +293,16 @@ __device__ __forceinline__ void regs_inc() {
 }
 
 // ------------------------------------------------------------------ math / packing
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start before the previous kernel in the stream ends;
+// griddep_wait() blocks until that kernel has completed and its memory is visible
+// (at once when there is none), griddep_launch_dependents() lets the next kernel
+// start launching.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
