@@ -660,6 +660,7 @@ __global__ void bwd_prep_kernel(const uint4* __restrict__ o, const uint4* __rest
                                 const float* __restrict__ lse, float* __restrict__ ws_delta,
                                 float* __restrict__ ws_lse2, float4* __restrict__ dq_acc, int BH,
                                 int N, int Np, size_t acc_vec4) {
+    griddep_wait();               // O, dO may come from the kernel before this one
     griddep_launch_dependents();  // the main kernel may launch and set up meanwhile
     const size_t tid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const size_t nthreads = static_cast<size_t>(gridDim.x) * blockDim.x;
@@ -763,10 +764,9 @@ int launch_bwd_impl(const void* q, const void* k, const void* v, const void* o, 
     int sms = 152, dev = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    bwd_prep_kernel<D><<<grid_for(static_cast<size_t>(BH) * Np * (D / 8), 256, sms * 8), 256, 0, s>>>(
-        static_cast<const uint4*>(o), static_cast<const uint4*>(dO), lse, ws_delta, ws_lse2,
-        reinterpret_cast<float4*>(dq_acc), BH, N, Np, acc_vec4);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(bwd_prep_kernel<D>, dim3(grid_for(static_cast<size_t>(BH) * Np * (D / 8), 256, sms * 8)),
+                               dim3(256), 0, s, static_cast<const uint4*>(o), static_cast<const uint4*>(dO), lse,
+                               ws_delta, ws_lse2, reinterpret_cast<float4*>(dq_acc), BH, N, Np, acc_vec4);
     if (e != cudaSuccess) return static_cast<int>(e);
 
     CUtensorMap tq, tk, tv, tdo;

@@ -255,6 +255,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
     const uint64_t lim = args.ctl.wait_ns;
+    // launched while the previous kernel in the stream may still run (its outputs may be
+    // these inputs): set up above, read nothing global before it has completed
+    griddep_wait();
+    griddep_launch_dependents();
 
     // 384 threads x 168 registers at launch: warpgroup 0 (load, MMA) gives up to
     // 120 per thread, the two softmax warpgroups take 184 (128*120 + 256*184 <= 384*168).
@@ -669,9 +673,19 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse
     a.qk_descale_k = kd;
     a.v_descale = vd;
     a.ctl = ctl;
-    dim3 grid(a.n_pairs * BH);
-    fwd_sm103_kernel<D, FP8, SHARD, PB><<<grid, kThreads, C::kSmemAlloc, s>>>(tq, tk, tv, to, a);
-    return static_cast<int>(cudaGetLastError());
+    // programmatic stream serialization: may start while the previous kernel finishes
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.n_pairs * BH);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::kSmemAlloc;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return static_cast<int>(
+        cudaLaunchKernelEx(&cfg, fwd_sm103_kernel<D, FP8, SHARD, PB>, tq, tk, tv, to, a));
 }
 
 }  // namespace
