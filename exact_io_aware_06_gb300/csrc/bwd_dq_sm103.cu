@@ -324,6 +324,8 @@ int launch_bwd_dq(const void* q, const void* k, const void* v, const void* dO,
     a.c_log2 = scale * 1.4426950408889634f;
     a.scale = scale;
     a.ctl = ctl;
+    // an ordinary launch: with programmatic serialization its CTAs would only sit
+    // waiting through the dK/dV kernel's tail (measured 0.3% slower)
     bwd_dq_kernel<128><<<a.n_q * BH, kThreads, C::kSmemAlloc, s>>>(tq, tk, tv, tdo, a);
     return static_cast<int>(cudaGetLastError());
 }

@@ -712,25 +712,6 @@ __global__ void bwd_dq_convert_kernel(const float4* __restrict__ acc, uint4* __r
     }
 }
 
-// Launch with programmatic stream serialization: the kernel may start while the
-// previous kernel in the stream finishes; it calls griddep_wait() before reading
-// that kernel's results.
-template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                       Args... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
-}
-
 int grid_for(size_t work, int threads, int max_blocks) {
     size_t b = (work + threads - 1) / threads;
     if (b > static_cast<size_t>(max_blocks)) b = max_blocks;

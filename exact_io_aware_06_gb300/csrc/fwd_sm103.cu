@@ -673,19 +673,8 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse
     a.qk_descale_k = kd;
     a.v_descale = vd;
     a.ctl = ctl;
-    // programmatic stream serialization: may start while the previous kernel finishes
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.n_pairs * BH);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = C::kSmemAlloc;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return static_cast<int>(
-        cudaLaunchKernelEx(&cfg, fwd_sm103_kernel<D, FP8, SHARD, PB>, tq, tk, tv, to, a));
+    return static_cast<int>(launch_pdl(fwd_sm103_kernel<D, FP8, SHARD, PB>, dim3(a.n_pairs * BH),
+                                       dim3(kThreads), C::kSmemAlloc, s, tq, tk, tv, to, a));
 }
 
 }  // namespace

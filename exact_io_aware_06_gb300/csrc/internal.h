@@ -21,6 +21,26 @@ struct DevCtl {
     uint64_t wait_ns;  // bound on one wait
 };
 
+// Launch with programmatic stream serialization: the kernel may start while the
+// previous kernel in the stream finishes (after a copy or an event it starts as
+// usual).  Every kernel launched this way calls griddep_wait() (ptx.cuh) before it
+// reads anything an earlier kernel may have written.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // fp32 exact forward on CUDA cores, d in {64, 128}.
 cudaError_t launch_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse,
                            int BH, int N, int d, float scale, int causal, cudaStream_t s);

@@ -35,6 +35,7 @@ __global__ void __launch_bounds__(256)
     constexpr int kVec = D / 4;         // lanes per row
     constexpr int kGroups = 32 / kVec;  // rows per warp
     static_assert(kVec >= kMaxParts, "a lane per part");
+    griddep_wait();  // the parts may come from the kernels just before this one
     const int lane = threadIdx.x & 31, j = lane % kVec, g = lane / kVec;
     const size_t warp = (static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
     const size_t step = static_cast<size_t>(gridDim.x) * blockDim.x / 32 * kGroups;
@@ -103,9 +104,8 @@ cudaError_t launch_merge_impl(const float* o_parts, const float* lse_parts, int 
     const size_t cap = static_cast<size_t>(sms) * per_sm;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    lse_merge_kernel<D, OUT_F32><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-        reinterpret_cast<const float4*>(o_parts), lse_parts, n_parts, rows, o, lse);
-    return cudaGetLastError();
+    return launch_pdl(lse_merge_kernel<D, OUT_F32>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s,
+                      reinterpret_cast<const float4*>(o_parts), lse_parts, n_parts, rows, o, lse);
 }
 
 }  // namespace
