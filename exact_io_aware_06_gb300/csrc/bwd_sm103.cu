@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         // ================================================================ producer
         if (lane == 0) {
             const uint32_t kvf = smem_u32(&bars.kv_full);
-            int g = 0, kc = 0;
+            int g = 0, kc = 0, kv_issued = 0;
             bool ok = true;
             for (int k = 0, x = item_x(0); x < n_items && ok; x = item_x(++k), ++kc) {
                 const Item I = item_at(x);
@@ -269,6 +269,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                     tma_load_3d(sb + kOffK + c * 16384, &tm_k, kvf, 64 * c, I.kvb * kBlk, I.bh);
                     tma_load_3d(sb + kOffV + c * 16384, &tm_v, kvf, 64 * c, I.kvb * kBlk, I.bh);
                 }
+                kv_issued = kc + 1;
                 for (int i = 0; i < I.n_it; ++i, ++g) {
                     const int s = g % kQStages;
                     const int qb = q_blk(I, i), qh = q_head(I, i);
@@ -289,9 +290,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                 }
             }
             if (!ok) record_timeout(args.ctl, &abort_flag);
-            // drain: the newest K/V load and the newest load of every stage have landed
+            // drain: the newest K/V load (also one issued by an item the loop then gave up
+            // on) and the newest load of every stage have landed
             const volatile int never = 0;
-            if (kc > 0) mbar_wait(kvf, (kc - 1) & 1, kDrainWaitNs, &never);
+            if (kv_issued > 0) mbar_wait(kvf, (kv_issued - 1) & 1, kDrainWaitNs, &never);
             for (int q = max(0, g - kQStages); q < g; ++q)
                 mbar_wait(smem_u32(&bars.q_full[q % kQStages]), (q / kQStages) & 1, kDrainWaitNs, &never);
         }
