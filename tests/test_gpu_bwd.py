@@ -95,3 +95,29 @@ def test_bwd_d128_b1_h8_n4096_sampled_heads(causal):
         for name, g, r in zip(("dq", "dk", "dv"), (dq[0, h], dk[0, h], dv[0, h]), ref):
             assert max_err(g, r) <= TOL_BF16_GRAD, name
     np.testing.assert_allclose(dv.sum(2), f64(x["do"]).sum(2), atol=0.25)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_back_to_back_backwards_share_a_workspace_without_host_sync(d):
+    # Two backward passes queued on one stream, one workspace, no synchronisation: the
+    # second pass's delta kernel (which zeroes the dQ accumulator) may start launching
+    # while the first pass's dQ conversion still reads that accumulator, and must wait
+    # for it.  Both passes' gradients are checked.
+    from exact_io_aware_06_gb300 import inputs
+    B, H, N = 1, 2, 300
+    s = scale_for(d)
+    x, dev = device_inputs(B, H, N, d, "bf16", with_do=True)
+    do2 = inputs.cast(inputs.normal((B, H, N, d), 91), "bf16")
+    q, k, v = dev["q"], dev["k"], dev["v"]
+    o, lse = fa.attention_forward(q, k, v, s, False)
+    ws = torch.empty(fa.fa_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device="cuda")
+    outs = []
+    for do in (dev["do"], do2.cuda()):
+        g = [torch.empty_like(q) for _ in range(3)]
+        fa.fa_bwd(q, k, v, o, lse, do, *g, ws, s, False, fa.FA_BF16)
+        outs.append(g)
+    check_status()
+    for do_host, g in zip((x["do"], do2), outs):
+        ref = oracle.attn_bwd(f64(x["q"]), f64(x["k"]), f64(x["v"]), f64(do_host), s, False)
+        for name, t, r in zip(("dq", "dk", "dv"), g, ref):
+            assert max_err(f64(t), r) <= TOL_BF16_GRAD, name

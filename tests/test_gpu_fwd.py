@@ -122,3 +122,33 @@ def test_bf16_deterministic_and_lse_optional():
     fa.fa_fwd(dev["q"], dev["k"], dev["v"], o3, None, s, True, fa.FA_BF16)
     check_status()
     assert torch.equal(o1, o3)
+
+
+# ---------------------------------------------------------------- back-to-back launches
+@pytest.mark.parametrize("d", [64, 128])
+def test_chained_forwards_ping_pong_without_host_sync(d):
+    # Kernels here may start while the one before them in the stream finishes (their
+    # set-up overlaps its tail), and must not read its output or overwrite what it reads
+    # until it has completed.  Stage t reads buffer A as Q and writes B; stage t + 1 reads
+    # B and writes A, which stage t was reading: both orders are exercised, on one stream,
+    # with no host synchronisation in between.  The oracle runs the same chain on its own
+    # outputs, rounded to bf16 between stages as the kernel's outputs are.
+    from exact_io_aware_06_gb300 import inputs
+    B, H, N = 2, 3, 300
+    s = scale_for(d)
+    q0 = inputs.cast(inputs.normal((B, H, N, d), 80), "bf16")
+    k = inputs.cast(inputs.normal((B, H, N, d), 81), "bf16")
+    v = inputs.cast(inputs.normal((B, H, N, d), 82), "bf16")
+    kd, vd = k.cuda(), v.cuda()
+    bufs = [q0.cuda(), torch.empty((B, H, N, d), dtype=torch.bfloat16, device="cuda")]
+    lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    stages = [False, True, False, True]  # causal flags
+    for t, causal in enumerate(stages):
+        fa.fa_fwd(bufs[t % 2], kd, vd, bufs[(t + 1) % 2], lse, s, causal, fa.FA_BF16)
+    check_status()
+    got = f64(bufs[len(stages) % 2])
+    ref = q0
+    for causal in stages:
+        o_ref, _ = oracle.attn_fwd(f64(ref), f64(k), f64(v), s, causal)
+        ref = torch.from_numpy(o_ref).to(torch.bfloat16)
+    assert max_err(got, f64(ref)) <= TOL_BF16_O
