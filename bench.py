@@ -61,19 +61,32 @@ def flops(kind, B, H, N, d, causal):
     return f / 2 if causal else f
 
 
-def dominant_traffic():
-    """DRAM bytes per launch of the dominant kernel from the committed ncu capture
-    (profiles/roofline_traffic.json), or None if its sources changed since."""
+def recorded_traffic(key):
+    """DRAM bytes per launch of one kernel (or one call's kernels) from the committed
+    ncu capture record ``profiles/roofline_traffic.json[key]``, or None if there is no
+    record or the sources it was taken on have changed since."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "roofline_traffic.json")
     if not os.path.exists(path):
         return None
-    rec = json.load(open(path))
+    rec = json.load(open(path)).get(key)
+    if rec is None:
+        return None
     h = hashlib.sha256()
     for f in rec["source_files"]:
         with open(os.path.join(ROOT, f), "rb") as fh:
             h.update(fh.read())
     return rec["traffic_bytes_per_launch"] if h.hexdigest() == rec["source_sha256"] else None
+
+
+def roofline_record(kernel, achieved, peak, peak_source, traffic_key, algorithmic_bytes):
+    """Roofline entry of a tensor-bound launch: achieved = algorithmic FLOP per launch over
+    its CUDA-event duration, against the measured peak of its dtype."""
+    return {"kernel": kernel, "bound": "tensor", "achieved": achieved, "peak": round(peak, 1),
+            "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "peak_source": peak_source,
+            "traffic": recorded_traffic(traffic_key),
+            "traffic_unit": "bytes per launch (ncu dram read+write)",
+            "algorithmic_bytes": algorithmic_bytes}
 
 
 def max_over_ranks(values, device=None):
@@ -467,7 +480,10 @@ def bench_ours(args):
     from exact_io_aware_06_gb300 import inputs
 
     stream = torch.cuda.current_stream()
-    parts = [make_part(torch, fa, inputs, p, dev) for p in PARTS]
+    chosen = [p for p in PARTS if not args.only or p[0] in args.only]
+    if not chosen:
+        raise SystemExit(f"--only names no part; parts are {[p[0] for p in PARTS]}")
+    parts = [make_part(torch, fa, inputs, p, dev) for p in chosen]
     torch.cuda.synchronize()
 
     def barrier():
@@ -511,8 +527,9 @@ def bench_ours(args):
                     [mids[k][i].elapsed_time(evs[k][i + 1]) for k in range(K)])
                 for i, P in enumerate(parts) if P["part"][1] == "fwdbwd"}
 
-    # e2e: same step with pinned host buffers, copies inside the timed region
-    Ke = max(3, K // 10)
+    # e2e: same step with pinned host buffers, copies inside the timed region; at least
+    # 10 steps whatever K is, so that the figure is stable at short runs
+    Ke = max(10, K // 10)
     pipe = E2EPipeline(torch, fa, parts, stream)
     pipe.step()
     pipe.join()
@@ -558,28 +575,54 @@ def bench_ours(args):
             part_out[name][sub] = {"ms": round(mean, 4), "tflops": round(tf, 1),
                                    "pct_of_peak": round(100 * tf / pk["bf16"], 1)}
 
-    dom = part_out[PARTS[0][0]]
-    roofline = {"kernel": "fwd_sm103_kernel<128,bf16> (B1 H32 N16384 d128 non-causal)",
-                "bound": "tensor", "achieved": dom["tflops"], "peak": pk["bf16"],
-                "unit": "TFLOP/s", "frac": round(dom["tflops"] / pk["bf16"], 4),
-                "peak_source": f"{pk['source']} bf16 burst (sustained {pk['bf16_sustained']})",
-                "traffic": dominant_traffic(),
-                "traffic_unit": "bytes per launch (ncu dram read+write)",
-                "algorithmic_bytes": 4 * 1 * 32 * 16384 * 128 * 2 + 32 * 16384 * 4}
+    # The step mixes bf16 and e4m3 stages: its peak is the FLOP-weighted one, i.e. the
+    # step's FLOP over the time every stage would take at its own dtype's peak.
+    peak_of = lambda dt: (fp8_tf or 2 * pk["bf16"]) if dt == "e4m3" else pk["bf16"]
+    ideal_s = sum(P["flop"] / (peak_of(P["part"][2]) * 1e12) for P in parts)
+    step_peak = step_flop / ideal_s / 1e12
+    dtypes = sorted({P["part"][2] for P in parts}, key=lambda t: t != "bf16")
+
+    rooflines = {}
+    if "fwd_bf16_b1h32n16384d128" in part_out:
+        rec = part_out["fwd_bf16_b1h32n16384d128"]
+        rooflines["fwd_bf16_b1h32n16384d128"] = roofline_record(
+            "fwd_sm103_kernel<128,bf16> (B1 H32 N16384 d128 non-causal), one launch",
+            rec["tflops"], pk["bf16"], f"{pk['source']} bf16 burst (sustained {pk['bf16_sustained']})",
+            "fwd_bf16_b1h32n16384d128", 4 * 1 * 32 * 16384 * 128 * 2 + 32 * 16384 * 4)
+    if "fwdbwd_bf16_b4h16n2048d64" in part_out:
+        rec = part_out["fwdbwd_bf16_b4h16n2048d64"]["bwd"]
+        n_elt = 4 * 16 * 2048 * 64
+        rooflines["bwd_bf16_b4h16n2048d64"] = roofline_record(
+            "fa_bwd d64 (B4 H16 N2048, non-causal): bwd_prep + bwd_main_kernel<64> + bwd_dq_convert",
+            rec["tflops"], pk["bf16"], f"{pk['source']} bf16 burst", "bwd_bf16_b4h16n2048d64",
+            8 * n_elt * 2 + 4 * 16 * 2048 * 4)
+    if "fwd_e4m3_b4h16n4096d128" in part_out and fp8_tf:
+        rec = part_out["fwd_e4m3_b4h16n4096d128"]
+        n_elt = 4 * 16 * 4096 * 128
+        rooflines["fwd_e4m3_b4h16n4096d128"] = roofline_record(
+            "fwd_sm103_kernel<128,e4m3> (B4 H16 N4096 d128 non-causal), one launch",
+            rec["tflops"], fp8_tf, "e4m3 torch._scaled_mm 8192^3 measured in this run",
+            "fwd_e4m3_b4h16n4096d128", 3 * n_elt + 2 * n_elt + 4 * 16 * 4096 * 4)
+    dominant = next(iter(rooflines.values()), None)
 
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "parallelism": "replicas" if world > 1 else "single",
+        "scaling": "weak", "vs_baseline": None, "dtype": "+".join(dtypes), "data": "synthetic",
+        "config": {"workload": WORKLOAD if not args.only else " + ".join(p[0] for p in chosen),
+                   "parallelism": "replicas" if world > 1 else "single",
                    "l2": "inputs larger than L2: each part follows a part that streams >129 MB"},
-        "pct_of_peak": round(100 * value / world / pk["bf16"], 1),
+        "pct_of_peak": round(100 * value / world / step_peak, 1),
+        "pct_of_peak_basis": (f"of the FLOP-weighted peak {step_peak:.1f} TFLOP/s: bf16 stages at "
+                              f"the measured bf16 burst {pk['bf16']}, e4m3 stages at the e4m3 peak "
+                              f"measured in this run ({None if fp8_tf is None else round(fp8_tf, 1)})"),
         "parts": part_out,
         "extras": extras,
         "fp8_peak_tflops": None if fp8_tf is None else round(fp8_tf, 1), "fp8_peak_how": fp8_how,
-        "roofline": roofline,
+        "roofline": dominant,
+        "rooflines": rooflines,
         "e2e": {"value": round(job_tflops(world, step_flop, e2e_ms), 1), "unit": UNIT,
-                "ms_per_step": round(e2e_ms, 3),
+                "ms_per_step": round(e2e_ms, 3), "steps": Ke,
                 "h2d_bytes_per_step": pipe.h2d, "d2h_bytes_per_step": pipe.d2h,
                 "copies": "pipelined: inputs in on one stream (double-buffered across steps), "
                           "outputs out on another, overlapping compute"},
@@ -636,6 +679,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--only", nargs="+", default=None, metavar="PART",
+                    help="run only these parts of the step (for profiling one kernel)")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the separately timed variant rows (``extras``)")
     args = ap.parse_args()

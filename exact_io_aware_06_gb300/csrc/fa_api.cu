@@ -245,7 +245,10 @@ __attribute__((visibility("default"))) int fa_lse_merge(const float* o_parts,
 }
 
 __attribute__((visibility("default"))) size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
+    // the product B*H is formed only once it is known to fit (the same bounds the
+    // backward itself enforces); sizes outside them have no workspace
     if (B < 1 || H < 1 || N < 1 || d < 1) return 0;
+    if (static_cast<int64_t>(B) * H > (1ll << 24) || N > (1 << 24)) return 0;
     return bwd_workspace_bytes(B * H, N, d);
 }
 

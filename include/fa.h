@@ -190,7 +190,8 @@ int fa_lse_merge(const float* o_parts, const float* lse_parts, int n_parts, void
  * delta_i = dO_i . O_i and the pre-scaled lse (float32, N rounded up to 128
  * per head), plus for d = 64 the float32 dQ accumulator
  * ([B][H][N rounded up to 128][d]).
- * Returns 0 for invalid sizes.
+ * Returns 0 for invalid sizes and for sizes the backward refuses
+ * (B*H > 2^24 or N > 2^24), whose byte count could overflow.
  */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 
