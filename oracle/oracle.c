@@ -272,28 +272,37 @@ ORACLE_API void oracle_bwd(const double* q, const double* k, const double* v,
                 dSi[j] = Pi[j] * (dp - dl);
             }
         }
-        /* dQ = scale dS K (row i of dQ needs row i of dS) */
+        /* dQ = scale dS K (row i of dQ needs row i of dS).  Each dQ_ic is the sum over
+         * j = 0, 1, ..., N-1 from 0.0; the loops run j outside c so that K is read by rows. */
 #pragma omp parallel for schedule(static)
         for (long i = 0; i < N; ++i) {
             const double* dSi = dS + (size_t)i * N;
-            for (long c = 0; c < d; ++c) {
-                double a = 0.0;
-                for (long j = 0; j < N; ++j) a += dSi[j] * kh[j * d + c];
-                dqh[i * d + c] = scale * a;
-            }
+            double* dqi = dqh + i * d;
+            for (long c = 0; c < d; ++c) dqi[c] = 0.0;
+            for (long j = 0; j < N; ++j)
+                for (long c = 0; c < d; ++c) dqi[c] += dSi[j] * kh[j * d + c];
+            for (long c = 0; c < d; ++c) dqi[c] *= scale;
         }
-        /* dV = P^T dO and dK = scale dS^T Q (row j needs column j of P and dS) */
-#pragma omp parallel for schedule(static)
-        for (long j = 0; j < N; ++j) {
-            for (long c = 0; c < d; ++c) {
-                double av = 0.0, ak = 0.0;
-                for (long i = 0; i < N; ++i) {
-                    av += P[(size_t)i * N + j] * doh[i * d + c];
-                    ak += dS[(size_t)i * N + j] * qh[i * d + c];
-                }
-                dvh[j * d + c] = av;
-                dkh[j * d + c] = scale * ak;
+        /* dV = P^T dO and dK = scale dS^T Q (row j needs column j of P and dS).  Each
+         * element is the sum over i = 0, 1, ..., N-1 from 0.0; a thread owns a range of
+         * rows j and runs i outside j, so P, dS, dO and Q are all read by rows. */
+#pragma omp parallel
+        {
+            const int nt = omp_get_num_threads(), t = omp_get_thread_num();
+            const long j0 = N * t / nt, j1 = N * (t + 1) / nt;
+            for (long j = j0; j < j1; ++j)
+                for (long c = 0; c < d; ++c) dvh[j * d + c] = dkh[j * d + c] = 0.0;
+            for (long i = 0; i < N; ++i) {
+                const double* Pi = P + (size_t)i * N;
+                const double* dSi = dS + (size_t)i * N;
+                for (long j = j0; j < j1; ++j)
+                    for (long c = 0; c < d; ++c) {
+                        dvh[j * d + c] += Pi[j] * doh[i * d + c];
+                        dkh[j * d + c] += dSi[j] * qh[i * d + c];
+                    }
             }
+            for (long j = j0; j < j1; ++j)
+                for (long c = 0; c < d; ++c) dkh[j * d + c] *= scale;
         }
     }
     free(P);

@@ -17,11 +17,11 @@ MUTANTS = {
                                "        if (causal && j >= i && j > 0) {\n            srow[j] = -INFINITY;"),
     "lse drops the max": ("    return m + log(l);", "    return log(l);"),
     "tiled rescale direction": ("exp(m[r] - ref)", "exp(ref - m[r])"),
-    "dV reads P transposed": ("av += P[(size_t)i * N + j] * doh[i * d + c];",
-                              "av += P[(size_t)j * N + i] * doh[i * d + c];"),
+    "dV reads P transposed": ("dvh[j * d + c] += Pi[j] * doh[i * d + c];",
+                              "dvh[j * d + c] += P[(size_t)j * N + i] * doh[i * d + c];"),
     "dS drops delta": ("dSi[j] = Pi[j] * (dp - dl);", "dSi[j] = Pi[j] * dp;"),
-    "dK misses the scale": ("dkh[j * d + c] = scale * ak;", "dkh[j * d + c] = ak;"),
-    "dQ uses V instead of K": ("a += dSi[j] * kh[j * d + c];", "a += dSi[j] * vh[j * d + c];"),
+    "dK misses the scale": ("dkh[j * d + c] *= scale;", "dkh[j * d + c] *= 1.0;"),
+    "dQ uses V instead of K": ("dqi[c] += dSi[j] * kh[j * d + c];", "dqi[c] += dSi[j] * vh[j * d + c];"),
     "E4M3 exponent bias": ("ldexp(1.0 + (double)mant / 8.0, e - 7)", "ldexp(1.0 + (double)mant / 8.0, e - 8)"),
 }
 
