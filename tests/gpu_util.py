@@ -64,3 +64,15 @@ def sample_rows(N, n_random=48, seed=0):
     rng = np.random.default_rng(seed)
     rnd = set(rng.integers(0, N, size=min(n_random, N)).tolist())
     return sorted(r for r in edges | rnd if 0 <= r < N)
+
+
+def head_rows(N, seed, n_random=4):
+    """Rows to check in every head of a large forward: the first and last row of the
+    first, middle and last 128-row query tiles (so both tiles of a CTA's pair and the
+    ragged end), plus a few random rows."""
+    last = (N - 1) // 128
+    mid = last // 2
+    edges = {0, 127, 128 * mid, 128 * mid + 127, 128 * last, N - 1}
+    rng = np.random.default_rng(1000 + seed)
+    rnd = set(rng.integers(0, N, size=min(n_random, N)).tolist())
+    return sorted(r for r in edges | rnd if 0 <= r < N)

@@ -37,22 +37,24 @@ def test_bwd_small(N, causal, d):
         assert max_err(f64(g), r) <= TOL_BF16_GRAD, name
 
 
-def test_bwd_config_b4_h16_n2048_d64_sampled_heads():
-    # the full backward workload; heads are independent, so whole heads are
-    # checked against the oracle
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_config_b4_h16_n2048_d64_every_head(causal):
+    # the full backward workload, every (b, h) compared element by element: the
+    # persistent kernel deals (head, key block) items to CTAs in alternating order,
+    # so covering every head covers every position of that schedule
     B, H, N, d = 4, 16, 2048, 64
     x, dev = device_inputs(B, H, N, d, "bf16", with_do=True)
     s = scale_for(d)
-    dq, dk, dv = (f64(t) for t in run_bwd(dev, s))
-    for t in (dq, dk, dv):
-        assert np.isfinite(t).all()
-    for b, h in ((0, 0), (3, 15)):
-        ref = oracle.attn_bwd(f64(x["q"][b, h]), f64(x["k"][b, h]), f64(x["v"][b, h]),
-                              f64(x["do"][b, h]), s)
-        for name, g, r in zip(("dq", "dk", "dv"), (dq[b, h], dk[b, h], dv[b, h]), ref):
-            assert max_err(g, r) <= TOL_BF16_GRAD, name
+    dq, dk, dv = (f64(t) for t in run_bwd(dev, s, causal))
+    ref = oracle.attn_bwd(f64(x["q"]), f64(x["k"]), f64(x["v"]), f64(x["do"]), s, causal)
+    for name, g, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+        err = np.abs(g - r).reshape(B * H, -1).max(axis=1)
+        assert err.max() <= TOL_BF16_GRAD, f"{name}: worst head {int(err.argmax())} {err.max():.3e}"
     # sum_j dV_j = sum_i dO_i holds for every head (rows of P sum to 1)
     np.testing.assert_allclose(dv.sum(2), f64(x["do"]).sum(2), atol=0.25)
+    if causal:
+        # query 0 sees only key 0: O_0 = V_0, so dS_00 = dO_0 . (V_0 - O_0) = 0 and dQ_0 = 0
+        assert np.abs(dq[:, :, 0]).max() <= 1e-2
 
 
 def test_bwd_workspace_reuse_and_determinism_of_dk_dv():
@@ -66,34 +68,18 @@ def test_bwd_workspace_reuse_and_determinism_of_dk_dv():
     assert max_err(f64(a[0]), f64(b[0])) <= 1e-2
 
 
-def test_bwd_causal_b4_h16_n2048_d64_sampled_heads():
-    # causal backward at the backward workload's size; whole heads against the oracle
-    B, H, N, d = 4, 16, 2048, 64
-    x, dev = device_inputs(B, H, N, d, "bf16", with_do=True)
-    s = scale_for(d)
-    dq, dk, dv = (f64(t) for t in run_bwd(dev, s, causal=True))
-    for b, h in ((0, 3), (2, 15)):
-        ref = oracle.attn_bwd(f64(x["q"][b, h]), f64(x["k"][b, h]), f64(x["v"][b, h]),
-                              f64(x["do"][b, h]), s, causal=True)
-        for name, g, r in zip(("dq", "dk", "dv"), (dq[b, h], dk[b, h], dv[b, h]), ref):
-            assert max_err(g, r) <= TOL_BF16_GRAD, name
-    # query 0 sees only key 0: O_0 = V_0, so dS_00 = dO_0 . (V_0 - O_0) = 0 and dQ_0 = 0
-    assert np.isfinite(dv).all() and np.isfinite(dq).all()
-    assert np.abs(dq[:, :, 0]).max() <= 1e-2
-
-
 @pytest.mark.parametrize("causal", [False, True])
-def test_bwd_d128_b1_h8_n4096_sampled_heads(causal):
+def test_bwd_d128_b1_h8_n4096_every_head(causal):
     # d = 128: key-parallel dK/dV kernel plus the query-parallel dQ kernel
     B, H, N, d = 1, 8, 4096, 128
     x, dev = device_inputs(B, H, N, d, "bf16", with_do=True)
     s = scale_for(d)
     dq, dk, dv = (f64(t) for t in run_bwd(dev, s, causal))
-    for h in (0, 5):
-        ref = oracle.attn_bwd(f64(x["q"][0, h]), f64(x["k"][0, h]), f64(x["v"][0, h]),
-                              f64(x["do"][0, h]), s, causal)
-        for name, g, r in zip(("dq", "dk", "dv"), (dq[0, h], dk[0, h], dv[0, h]), ref):
-            assert max_err(g, r) <= TOL_BF16_GRAD, name
+    # every head, element by element
+    ref = oracle.attn_bwd(f64(x["q"]), f64(x["k"]), f64(x["v"]), f64(x["do"]), s, causal)
+    for name, g, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+        err = np.abs(g - r).reshape(B * H, -1).max(axis=1)
+        assert err.max() <= TOL_BF16_GRAD, f"{name}: worst head {int(err.argmax())} {err.max():.3e}"
     np.testing.assert_allclose(dv.sum(2), f64(x["do"]).sum(2), atol=0.25)
 
 

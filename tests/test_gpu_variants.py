@@ -7,7 +7,7 @@ import torch
 import exact_io_aware_06_gb300 as fa
 import oracle
 from exact_io_aware_06_gb300 import inputs
-from gpu_util import (TOL_BF16_O, TOL_FP8_O, TOL_LSE_BF16, TOL_LSE_FP8, check_status, ensure_built,
+from gpu_util import (head_rows, TOL_BF16_O, TOL_FP8_O, TOL_LSE_BF16, TOL_LSE_FP8, check_status, ensure_built,
                       f64, max_err, sample_rows, scale_for)
 
 pytestmark = pytest.mark.gpu
@@ -214,3 +214,31 @@ def test_fp8_per_block_b4_h16_n4096_d128_sampled():
         assert np.isfinite(o).all()
         for b, h in ((0, 0), (2, 7), (3, 15)):
             check_per_block_head(x, o, lse, b, h, sample_rows(N, 24, seed=b * 16 + h), causal, d)
+
+
+# ---------------------------------------------------------------- finer factors, plain inputs
+@pytest.mark.parametrize("granularity", ["head", "block"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_finer_factors_iid_normal_meet_the_plain_bound(granularity, causal):
+    # The FP8 workload's own inputs (iid N(0,1), B4 H16 N4096 d128) quantised with one
+    # factor per head or per 128-row block: the plain FP8 bound (max abs 1e-1 on O) holds,
+    # as it does with one factor per tensor.  Every head, tile-edge and random rows.
+    B, H, N, d = 4, 16, 4096, 128
+    quant = inputs.quantize_e4m3_per_head if granularity == "head" else inputs.quantize_e4m3_per_block
+    x = {}
+    for i, n in enumerate("qkv"):
+        x[n], x[n + "_descale"] = quant(inputs.normal((B, H, N, d), 42 + i))
+    o, lse = (run_fp8_per_head if granularity == "head" else run_fp8_per_block)(x, causal)
+    assert np.isfinite(o).all()
+    for b in range(B):
+        for h in range(H):
+            rows = head_rows(N, b * H + h)
+            if granularity == "head":
+                qh, kh, vh = (dequant_head(x, n, b, h) for n in "qkv")
+            else:
+                qh, kh, vh = (oracle.e4m3_decode_blocks(x[n][b, h].numpy(),
+                                                        x[n + "_descale"][b, h].numpy())
+                              for n in "qkv")
+            o_ref, lse_ref = oracle.attn_fwd_rows(qh, kh, vh, rows, scale_for(d), causal)
+            assert max_err(o[b, h, rows], o_ref) <= TOL_FP8_O, f"b{b} h{h}"
+            assert max_err(lse[b, h, rows], lse_ref) <= TOL_LSE_FP8, f"b{b} h{h}"
