@@ -217,12 +217,17 @@ def test_fp8_per_block_b4_h16_n4096_d128_sampled():
 
 
 # ---------------------------------------------------------------- finer factors, plain inputs
-@pytest.mark.parametrize("granularity", ["head", "block"])
-@pytest.mark.parametrize("causal", [False, True])
-def test_fp8_finer_factors_iid_normal_meet_the_plain_bound(granularity, causal):
+@pytest.mark.parametrize("granularity,causal", [("head", False), ("head", True), ("block", False),
+                                                ("block", True)])
+def test_fp8_finer_factors_iid_normal(granularity, causal):
     # The FP8 workload's own inputs (iid N(0,1), B4 H16 N4096 d128) quantised with one
-    # factor per head or per 128-row block: the plain FP8 bound (max abs 1e-1 on O) holds,
-    # as it does with one factor per tensor.  Every head, tile-edge and random rows.
+    # factor per head or per 128-row block; every head, tile-edge and random rows.
+    # The plain FP8 bound (max abs 1e-1 on O) holds for per-head factors, as for one
+    # factor per tensor, and for per-block factors without the mask.  Per-block causal
+    # rows that see only a few keys do not average the E4M3 rounding of P r_j (V's block
+    # factor folded into P): row 0 returns e4m3(r_0) vd_max V8_0 for vd_0 V8_0, off by up
+    # to 2^-4 |V_0| (measured 0.117 on these inputs), so there the per-row bound derived
+    # from the kernel's arithmetic (per_block_bound) applies instead.
     B, H, N, d = 4, 16, 4096, 128
     quant = inputs.quantize_e4m3_per_head if granularity == "head" else inputs.quantize_e4m3_per_block
     x = {}
@@ -233,6 +238,9 @@ def test_fp8_finer_factors_iid_normal_meet_the_plain_bound(granularity, causal):
     for b in range(B):
         for h in range(H):
             rows = head_rows(N, b * H + h)
+            if granularity == "block" and causal:
+                check_per_block_head(x, o, lse, b, h, rows, causal, d)
+                continue
             if granularity == "head":
                 qh, kh, vh = (dequant_head(x, n, b, h) for n in "qkv")
             else:
