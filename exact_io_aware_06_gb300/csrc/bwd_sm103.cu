@@ -19,7 +19,10 @@
 //   3. bwd_dq_convert  dQ = bf16(scale * accumulator).
 //
 // bwd_main layout (d = 64), 16 warps:
-//   warp 0      TMA producer: K_j, V_j once; Q_i, dO_i, lse_i, delta_i in a 3-stage ring
+//   warp 0      TMA producer: Q_i, dO_i, lse_i, delta_i in a 3-stage ring that runs
+//               across item boundaries
+//   warp 3      TMA producer: K_j (two buffers: the next item's K loads while this item
+//               runs) and V_j (reloaded as soon as the item's last dP has read it)
 //   warp 1      MMA issuer (dV, S, dK, dP) + TMEM owner
 //   warp 2      second MMA issuer: dQ (d = 64 only)
 //   warps 4-7   P/dS for query columns 0-63 of block i   (thread = key row)
@@ -38,6 +41,7 @@
 //     dQ_i = dS_i K_j         (SS, dS from smem MN-major, K_j MN-major; warp 2)
 //   so the next block's scores are ready when the P/dS warps finish dS_i.
 #include <cmath>
+#include <type_traits>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -90,8 +94,11 @@ struct BwdCfg {
     static constexpr int kChunks = D / 64;                    // 128-byte swizzle columns per row
     static constexpr int kTile = kBlk * D * 2;                // bf16 128 x D tile
     // shared memory map (offsets from a 1 KB aligned base)
-    static constexpr int kOffK = 0;
-    static constexpr int kOffV = kOffK + kTile;
+    // d = 64: two K buffers, so the next item's K loads while this item runs (V, read only
+    // by dP, is released one block before the end of an item and reloads in place)
+    static constexpr int kKBufs = kFusedDQ ? 2 : 1;
+    static constexpr int kOffK = 0;                            // kKBufs
+    static constexpr int kOffV = kOffK + kKBufs * kTile;
     static constexpr int kOffQ = kOffV + kTile;               // kQStages
     static constexpr int kOffDO = kOffQ + kQStages * kTile;   // kQStages
     static constexpr int kDSBytes = kBlk * kBlk * 2;
@@ -126,7 +133,8 @@ struct BwdArgs {
 
 template <int NQ>
 struct Bars {
-    uint64_t kv_full, kv_empty;  // the K/V tile of the current item
+    uint64_t k_full[2], k_empty[2];  // K buffer (item kc uses buffer kc % kKBufs)
+    uint64_t v_full, v_empty;        // the V tile
     uint64_t q_full[NQ], q_empty[NQ];
     uint64_t s_full, dp_full, p_full;
     uint64_t ds_full[2];  // dS_i written (TMEM and dS buffer i % 2); one barrier per buffer
@@ -203,9 +211,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
-        mbar_init(smem_u32(&bars.kv_full), 1);
-        // the K/V tile is free again once every thread that reads it has committed
-        mbar_init(smem_u32(&bars.kv_empty), C::kFusedDQ ? 2 : 1);
+        // a K buffer is free again once every thread that reads it has committed (the
+        // main MMA thread after the item's last S, the dQ thread after its last dQ); V once
+        // the main thread's last dP of the item has completed
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&bars.k_full[b]), 1);
+            mbar_init(smem_u32(&bars.k_empty[b]), C::kFusedDQ ? 2 : 1);
+        }
+        mbar_init(smem_u32(&bars.v_full), 1);
+        mbar_init(smem_u32(&bars.v_empty), 1);
         for (int s = 0; s < kQStages; ++s) {
             mbar_init(smem_u32(&bars.q_full[s]), 1);
             mbar_init(smem_u32(&bars.q_empty[s]), 1);
@@ -252,24 +266,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     griddep_launch_dependents();
 
     if (warp == 0) {
-        // ================================================================ producer
+        // ================================================================ Q / dO producer
+        // The ring runs across item boundaries: it waits only for its own stages.
         if (lane == 0) {
-            const uint32_t kvf = smem_u32(&bars.kv_full);
-            int g = 0, kc = 0, kv_issued = 0;
+            int g = 0;
             bool ok = true;
-            for (int k = 0, x = item_x(0); x < n_items && ok; x = item_x(++k), ++kc) {
+            for (int k = 0, x = item_x(0); x < n_items && ok; x = item_x(++k)) {
                 const Item I = item_at(x);
-                // this item's K/V over the previous item's, once that one is consumed
-                if (kc > 0 && !mbar_wait(smem_u32(&bars.kv_empty), (kc - 1) & 1, lim, &abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                mbar_arrive_expect_tx(kvf, 2 * kTile);
-                for (int c = 0; c < kChunks; ++c) {  // 64-column swizzle chunks, 16 KB apart
-                    tma_load_3d(sb + kOffK + c * 16384, &tm_k, kvf, 64 * c, I.kvb * kBlk, I.bh);
-                    tma_load_3d(sb + kOffV + c * 16384, &tm_v, kvf, 64 * c, I.kvb * kBlk, I.bh);
-                }
-                kv_issued = kc + 1;
                 for (int i = 0; i < I.n_it; ++i, ++g) {
                     const int s = g % kQStages;
                     const int qb = q_blk(I, i), qh = q_head(I, i);
@@ -290,17 +293,55 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                 }
             }
             if (!ok) record_timeout(args.ctl, &abort_flag);
-            // drain: the newest K/V load (also one issued by an item the loop then gave up
-            // on) and the newest load of every stage have landed
+            // drain: the newest load of every stage has landed
             const volatile int never = 0;
-            if (kv_issued > 0) mbar_wait(kvf, (kv_issued - 1) & 1, kDrainWaitNs, &never);
             for (int q = max(0, g - kQStages); q < g; ++q)
                 mbar_wait(smem_u32(&bars.q_full[q % kQStages]), (q / kQStages) & 1, kDrainWaitNs, &never);
+        }
+    } else if (warp == 3) {
+        // ================================================================ K / V producer
+        // Item kc's K goes into buffer kc % kKBufs once that buffer's previous item has
+        // released it (with two buffers: as soon as the item before this CTA's current one
+        // ends); its V once the previous item's last dP has completed.
+        if (lane == 0) {
+            constexpr int kKB = C::kKBufs;
+            int k_issued = 0, v_issued = 0;
+            bool ok = true;
+            for (int kc = 0, x = item_x(0); x < n_items; x = item_x(++kc)) {
+                const Item I = item_at(x);
+                const int b = kc % kKB, u = kc / kKB;
+                if (u > 0 && !mbar_wait(smem_u32(&bars.k_empty[b]), (u - 1) & 1, lim, &abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t kf = smem_u32(&bars.k_full[b]);
+                mbar_arrive_expect_tx(kf, kTile);
+                for (int c = 0; c < kChunks; ++c)
+                    tma_load_3d(sb + kOffK + b * kTile + c * 16384, &tm_k, kf, 64 * c, I.kvb * kBlk, I.bh);
+                k_issued = kc + 1;
+                if (kc > 0 && !mbar_wait(smem_u32(&bars.v_empty), (kc - 1) & 1, lim, &abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t vf = smem_u32(&bars.v_full);
+                mbar_arrive_expect_tx(vf, kTile);
+                for (int c = 0; c < kChunks; ++c)
+                    tma_load_3d(sb + kOffV + c * 16384, &tm_v, vf, 64 * c, I.kvb * kBlk, I.bh);
+                v_issued = kc + 1;
+            }
+            if (!ok) record_timeout(args.ctl, &abort_flag);
+            // drain: the newest K load of each buffer and the newest V load have landed
+            // (also loads for an item the consumers then gave up on)
+            const volatile int never = 0;
+            for (int kc = max(0, k_issued - kKB); kc < k_issued; ++kc)
+                mbar_wait(smem_u32(&bars.k_full[kc % kKB]), (kc / kKB) & 1, kDrainWaitNs, &never);
+            if (v_issued > 0) mbar_wait(smem_u32(&bars.v_full), (v_issued - 1) & 1, kDrainWaitNs, &never);
         }
     } else if (warp == 1) {
         // ================================================================ MMA issuer
         if (lane == 0) {
-            const uint32_t sK = sb + kOffK, sV = sb + kOffV;
+            const uint32_t sV = sb + kOffV;
+            uint32_t sK = sb + kOffK;  // this item's K buffer
             auto issue_s = [&](int s) {  // S^T = K_j Q^T into columns 0-127
                 const uint32_t sQ = sb + kOffQ + s * kTile;
 #pragma unroll
@@ -325,28 +366,43 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             bool ok = true;
             for (int k = 0, x = item_x(0); x < n_items && ok; x = item_x(++k), ++kc) {
                 const Item I = item_at(x);
+                const int kb = kc % C::kKBufs;
+                sK = sb + kOffK + kb * kTile;
                 // the item's first scores; S and dP of the previous item's last block were
-                // read by its dV and dK, issued before these by this thread
-                ok = mbar_wait(smem_u32(&bars.kv_full), kc & 1, lim, &abort_flag);
+                // read by its dV and dK, issued before these by this thread.  K and V are
+                // released after their last readers: K after the item's last S (and, d = 64,
+                // the dQ thread's last dQ), V after its last dP.
+                ok = mbar_wait(smem_u32(&bars.k_full[kb]), (kc / C::kKBufs) & 1, lim, &abort_flag);
                 if (ok) ok = mbar_wait(smem_u32(&bars.q_full[g % kQStages]), (g / kQStages) & 1, lim, &abort_flag);
                 if (!ok) break;
                 tc_fence_after();
                 issue_s(g % kQStages);
+                if (I.n_it == 1) mma_commit(smem_u32(&bars.k_empty[kb]));
+                ok = mbar_wait(smem_u32(&bars.v_full), kc & 1, lim, &abort_flag);
+                if (!ok) break;
+                tc_fence_after();
                 issue_dp(g % kQStages);
-                for (int i = 0; i < I.n_it; ++i) {
+                if (I.n_it == 1) mma_commit(smem_u32(&bars.v_empty));
+                // One query block: dV_i, the next block's S, dK_i, the next block's dP.  MORE:
+                // a next block exists; LAST2: that next block is the item's last, so this
+                // block issues the item's last S and dP and releases K and V after them.
+                // The two flags are compile-time: the item's last two blocks run outside the
+                // loop, which keeps the loop body free of the release commits (a conditional
+                // commit inside it measured ~100 cycles slower per block).
+                auto block = [&](int i, auto more_c, auto last2_c) -> bool {
+                    constexpr bool more = decltype(more_c)::value, last2 = decltype(last2_c)::value;
                     const int gi = g + i;
                     const int s = gi % kQStages;
                     const int s1 = (gi + 1) % kQStages;
-                    const bool more = i + 1 < I.n_it;
                     const uint32_t sQ = sb + kOffQ + s * kTile, sDO = sb + kOffDO + s * kTile;
                     // The loads of block i+1 (ready blocks ahead) are checked together with
                     // P_i: every wait of an issuing thread can leave the tensor pipe idle.
                     // P of an item's first block is computed after the P/dS warps have read
                     // the previous item's dV and dK, so dV, dK may then be overwritten.
-                    ok = mbar_wait(smem_u32(&bars.p_full), gi & 1, lim, &abort_flag);
-                    if (ok && more)
-                        ok = mbar_wait(smem_u32(&bars.q_full[s1]), ((gi + 1) / kQStages) & 1, lim, &abort_flag);
-                    if (!ok) break;
+                    bool okb = mbar_wait(smem_u32(&bars.p_full), gi & 1, lim, &abort_flag);
+                    if (okb && more)
+                        okb = mbar_wait(smem_u32(&bars.q_full[s1]), ((gi + 1) / kQStages) & 1, lim, &abort_flag);
+                    if (!okb) return false;
                     tc_fence_after();
                     // dV += P^T dO_i
 #pragma unroll
@@ -354,11 +410,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                         mma_bf16_ts(tmem + kColDV, tmem + kColS + 64 * (kk >> 2) + 8 * (kk & 3),
                                     sdesc_sw128(sDO + 2048 * kk, 16384, 1024), kIdescTS, (i > 0) || (kk > 0));
                     // next block's scores: the P/dS warps keep P_i in registers
-                    if (more) issue_s(s1);
+                    if constexpr (more) {
+                        issue_s(s1);
+                        if constexpr (last2) mma_commit(smem_u32(&bars.k_empty[kb]));  // K's last S
+                    }
                     // one barrier per dS buffer: writing buffer gi % 2 again needs block gi's
                     // dK and dQ, so no waiter can fall two phases behind
-                    ok = mbar_wait(smem_u32(&bars.ds_full[gi & 1]), (gi >> 1) & 1, lim, &abort_flag);
-                    if (!ok) break;
+                    if (!mbar_wait(smem_u32(&bars.ds_full[gi & 1]), (gi >> 1) & 1, lim, &abort_flag))
+                        return false;
                     tc_fence_after();
                     // dK += dS^T Q_i
 #pragma unroll
@@ -366,11 +425,20 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                         mma_bf16_ts(tmem + kColDK, tmem + kColDP + 64 * (kk >> 2) + 8 * (kk & 3),
                                     sdesc_sw128(sQ + 2048 * kk, 16384, 1024), kIdescTS, (i > 0) || (kk > 0));
                     mma_commit(smem_u32(&bars.q_empty[s]));  // Q_i, dO_i, lse_i, delta_i consumed
-                    if (more) issue_dp(s1);
-                }
+                    if constexpr (more) {
+                        issue_dp(s1);
+                        if constexpr (last2) mma_commit(smem_u32(&bars.v_empty));  // V's last dP
+                    }
+                    return true;
+                };
+                using T = std::true_type;
+                using F = std::false_type;
+                int i = 0;
+                for (; i + 2 < I.n_it && ok; ++i) ok = block(i, T{}, F{});
+                if (ok && I.n_it >= 2) ok = block(I.n_it - 2, T{}, T{});
+                if (ok) ok = block(I.n_it - 1, F{}, F{});
                 if (!ok) break;
                 mma_commit(smem_u32(&bars.all_done));  // the item's dV, dK are final
-                mma_commit(smem_u32(&bars.kv_empty));  // this thread's reads of K, V are done
                 g += I.n_it;
             }
             if (!ok) record_timeout(args.ctl, &abort_flag);
@@ -385,12 +453,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         // stall the main MMA chain, and its MMAs read nothing that chain writes (dS in
         // shared memory, K) and write only the dQ buffers.
         if (lane == 0) {
-            const uint32_t sK = sb + kOffK;
             int g = 0, kc = 0;
             bool ok = true;
             for (int k = 0, x = item_x(0); x < n_items && ok; x = item_x(++k), ++kc) {
                 const Item I = item_at(x);
-                ok = mbar_wait(smem_u32(&bars.kv_full), kc & 1, lim, &abort_flag);
+                const int kb = kc % C::kKBufs;
+                const uint32_t sK = sb + kOffK + kb * kTile;
+                ok = mbar_wait(smem_u32(&bars.k_full[kb]), (kc / C::kKBufs) & 1, lim, &abort_flag);
                 for (int i = 0; i < I.n_it && ok; ++i) {
                     const int gi = g + i, b = gi & 1;
                     ok = mbar_wait(smem_u32(&bars.ds_full[b]), (gi >> 1) & 1, lim, &abort_flag);
@@ -406,7 +475,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                     mma_commit(smem_u32(&bars.dq_full[b]));  // also: dS buffer b consumed
                 }
                 if (!ok) break;
-                mma_commit(smem_u32(&bars.kv_empty));  // this thread's reads of K are done
+                mma_commit(smem_u32(&bars.k_empty[kb]));  // this thread's reads of K are done
                 g += I.n_it;
             }
             if (!ok) record_timeout(args.ctl, &abort_flag);
@@ -656,61 +725,100 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 // -delta_i = -(dO_i . O_i) and -lse_i * log2(e) (rows past N: 0 and -inf, so
 // that recomputed P is exactly 0 there), dQ accumulator zeroed.  Both are stored
 // negated so the main kernel adds them with packed FMA/FADD.
-// D/8 threads per row, each reading 16 bytes of O and dO.
+// D/8 lanes per row, each reading 16 bytes of O and of dO; a thread works on kRows
+// rows at once (all their loads in flight before the first use) and zeroes the same
+// rows of the accumulator, so the pass streams at close to the memory rate.
 template <int D>
-__global__ void bwd_prep_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dO,
-                                const float* __restrict__ lse, float* __restrict__ ws_delta,
-                                float* __restrict__ ws_lse2, float4* __restrict__ dq_acc, int BH,
-                                int N, int Np, size_t acc_vec4) {
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dO,
+                                                       const float* __restrict__ lse, float* __restrict__ ws_delta,
+                                                       float* __restrict__ ws_lse2, float4* __restrict__ dq_acc,
+                                                       int BH, int N, int Np) {
     griddep_wait();               // O, dO may come from the kernel before this one
     griddep_launch_dependents();  // the main kernel may launch and set up meanwhile
-    const size_t tid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const size_t nthreads = static_cast<size_t>(gridDim.x) * blockDim.x;
+    constexpr int kT = D / 8;              // lanes per row (8 or 16): the shuffles stay in a warp
+    constexpr int kRowsPerWarp = 32 / kT;  // rows one warp covers per step
+    constexpr int kRows = 4;               // steps in flight per thread
+    const int lane = threadIdx.x & 31, part = lane % kT, sub = lane / kT;
+    const size_t warps = static_cast<size_t>(gridDim.x) * (blockDim.x / 32);
+    const size_t wid = static_cast<size_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
     const size_t rows = static_cast<size_t>(BH) * Np;
-    constexpr int kT = D / 8;  // threads per row (8 or 16): the shuffles stay inside a warp
-    for (size_t base = tid; base < rows * kT; base += nthreads) {
-        const size_t r = base / kT;
-        const int part = static_cast<int>(base % kT);
-        const int bh = static_cast<int>(r / Np), i = static_cast<int>(r % Np);
-        float sum = 0.f;
-        if (i < N) {
+    const size_t per_iter = static_cast<size_t>(kRowsPerWarp) * kRows;
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (size_t r0 = wid * per_iter; r0 < rows; r0 += warps * per_iter) {
+        uint4 a[kRows], b[kRows];
+        bool valid[kRows];
+#pragma unroll
+        for (int u = 0; u < kRows; ++u) {
+            const size_t r = r0 + static_cast<size_t>(u) * kRowsPerWarp + sub;
+            const int bh = static_cast<int>(r / Np), i = static_cast<int>(r % Np);
+            valid[u] = r < rows && i < N;
             const size_t src = (static_cast<size_t>(bh) * N + i) * kT + part;
-            const uint4 a = o[src], b = dO[src];
-            const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+            a[u] = valid[u] ? o[src] : make_uint4(0u, 0u, 0u, 0u);
+            b[u] = valid[u] ? dO[src] : make_uint4(0u, 0u, 0u, 0u);
+        }
+        if (dq_acc != nullptr) {
+#pragma unroll
+            for (int u = 0; u < kRows; ++u) {
+                const size_t r = r0 + static_cast<size_t>(u) * kRowsPerWarp + sub;
+                if (r < rows) {  // D floats per row: D/4 float4, kT lanes -> 2 each
+                    dq_acc[r * (D / 4) + 2 * part] = z;
+                    dq_acc[r * (D / 4) + 2 * part + 1] = z;
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kRows; ++u) {
+            const uint32_t av[4] = {a[u].x, a[u].y, a[u].z, a[u].w}, bv[4] = {b[u].x, b[u].y, b[u].z, b[u].w};
+            float sum = 0.f;
 #pragma unroll
             for (int x = 0; x < 4; ++x) {
                 sum = fmaf(__uint_as_float(av[x] << 16), __uint_as_float(bv[x] << 16), sum);
                 sum = fmaf(__uint_as_float(av[x] & 0xFFFF0000u), __uint_as_float(bv[x] & 0xFFFF0000u), sum);
             }
-        }
-        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-        if (kT == 16) sum += __shfl_xor_sync(0xffffffffu, sum, 8);
-        if (part == 0) {
-            ws_delta[r] = -sum;
-            ws_lse2[r] = (i < N) ? -lse[static_cast<size_t>(bh) * N + i] * kLog2e : -INFINITY;
+            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+            if (kT == 16) sum += __shfl_xor_sync(0xffffffffu, sum, 8);
+            const size_t r = r0 + static_cast<size_t>(u) * kRowsPerWarp + sub;
+            if (part == 0 && r < rows) {
+                const int bh = static_cast<int>(r / Np), i = static_cast<int>(r % Np);
+                ws_delta[r] = -sum;
+                ws_lse2[r] = valid[u] ? -lse[static_cast<size_t>(bh) * N + i] * kLog2e : -INFINITY;
+            }
         }
     }
-    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (size_t x = tid; x < acc_vec4; x += nthreads) dq_acc[x] = z;
 }
 
-// dQ = bf16(scale * accumulator) for rows < N (d = 64); 8 elements per thread.
-__global__ void bwd_dq_convert_kernel(const float4* __restrict__ acc, uint4* __restrict__ dq,
-                                      int N, int Np, size_t n_vec8, float scale) {
+// dQ = bf16(scale * accumulator) for rows < N (d = 64); 8 elements per thread, kVecs
+// groups in flight per thread.
+__global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float4* __restrict__ acc, uint4* __restrict__ dq,
+                                                             int N, int Np, size_t n_vec8, float scale) {
     griddep_wait();  // launched while the main kernel may still run
-    const size_t tid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    constexpr int kVecs = 4;
     const size_t nthreads = static_cast<size_t>(gridDim.x) * blockDim.x;
     constexpr int kVecPerRow = 64 / 8;
-    for (size_t x = tid; x < n_vec8; x += nthreads) {
-        const size_t row = x / kVecPerRow;  // row in [BH][N]
-        const int part = static_cast<int>(x % kVecPerRow);
-        const size_t bh = row / N, i = row % N;
-        const size_t src = ((bh * Np + i) * kVecPerRow + part) * 2;
-        const float4 a = acc[src], b = acc[src + 1];
-        dq[x] = make_uint4(pack_bf16x2(a.x * scale, a.y * scale), pack_bf16x2(a.z * scale, a.w * scale),
-                           pack_bf16x2(b.x * scale, b.y * scale), pack_bf16x2(b.z * scale, b.w * scale));
+    for (size_t x0 = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; x0 < n_vec8;
+         x0 += nthreads * kVecs) {
+        float4 a[kVecs], b[kVecs];
+#pragma unroll
+        for (int u = 0; u < kVecs; ++u) {
+            const size_t x = x0 + u * nthreads;
+            if (x < n_vec8) {
+                const size_t row = x / kVecPerRow;  // row in [BH][N]
+                const int part = static_cast<int>(x % kVecPerRow);
+                const size_t bh = row / N, i = row % N;
+                const size_t src = ((bh * Np + i) * kVecPerRow + part) * 2;
+                a[u] = acc[src];
+                b[u] = acc[src + 1];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kVecs; ++u) {
+            const size_t x = x0 + u * nthreads;
+            if (x < n_vec8)
+                dq[x] = make_uint4(pack_bf16x2(a[u].x * scale, a[u].y * scale), pack_bf16x2(a[u].z * scale, a[u].w * scale),
+                                   pack_bf16x2(b[u].x * scale, b[u].y * scale), pack_bf16x2(b[u].z * scale, b[u].w * scale));
+        }
     }
 }
 
@@ -742,14 +850,15 @@ int launch_bwd_impl(const void* q, const void* k, const void* v, const void* o, 
     float* ws_delta = ws;
     float* ws_lse2 = ws + static_cast<size_t>(BH) * Np;
     float* dq_acc = C::kFusedDQ ? ws + 2 * static_cast<size_t>(BH) * Np : nullptr;
-    const size_t acc_vec4 = C::kFusedDQ ? static_cast<size_t>(BH) * Np * D / 4 : 0;
 
     int sms = 152, dev = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaError_t e = launch_pdl(bwd_prep_kernel<D>, dim3(grid_for(static_cast<size_t>(BH) * Np * (D / 8), 256, sms * 8)),
-                               dim3(256), 0, s, static_cast<const uint4*>(o), static_cast<const uint4*>(dO), lse,
-                               ws_delta, ws_lse2, reinterpret_cast<float4*>(dq_acc), BH, N, Np, acc_vec4);
+    // prep: a warp covers 32/(D/8) rows per step and 4 steps at once
+    const size_t prep_warps = (static_cast<size_t>(BH) * Np + (32 / (D / 8)) * 4 - 1) / ((32 / (D / 8)) * 4);
+    cudaError_t e = launch_pdl(bwd_prep_kernel<D>, dim3(grid_for(prep_warps * 32, 256, sms * 8)), dim3(256), 0, s,
+                               static_cast<const uint4*>(o), static_cast<const uint4*>(dO), lse, ws_delta, ws_lse2,
+                               reinterpret_cast<float4*>(dq_acc), BH, N, Np);
     if (e != cudaSuccess) return static_cast<int>(e);
 
     CUtensorMap tq, tk, tv, tdo;
@@ -792,13 +901,23 @@ int launch_bwd_impl(const void* q, const void* k, const void* v, const void* o, 
     // persistent: one CTA per SM (fewer if there are fewer items), each looping over items
     const int n_items = a.n_kv * BH_kv;
     const int grid = n_items < sms ? n_items : sms;
-    e = launch_pdl(bwd_main_kernel<D>, dim3(grid), dim3(C::kThreads), C::kSmemAlloc, s, tq, tk, tv,
-                   tdo, tdq, tdk, tdv, a);
+    // Non-causal: launched with programmatic serialization, so its set-up overlaps the
+    // delta pass.  Causal: an ordinary launch.  The causal items are dealt heaviest first
+    // on the assumption that every CTA starts together; under programmatic launch the
+    // CTAs start as the delta pass drains from their SMs, and the staggered start left
+    // the heavy items' CTAs ~10% behind (B4 H16 N2048 d64: 146 -> 133 us).
+    if (causal) {
+        bwd_main_kernel<D><<<grid, C::kThreads, C::kSmemAlloc, s>>>(tq, tk, tv, tdo, tdq, tdk, tdv, a);
+        e = cudaGetLastError();
+    } else {
+        e = launch_pdl(bwd_main_kernel<D>, dim3(grid), dim3(C::kThreads), C::kSmemAlloc, s, tq, tk, tv,
+                       tdo, tdq, tdk, tdv, a);
+    }
     if (e != cudaSuccess) return static_cast<int>(e);
 
     if constexpr (C::kFusedDQ) {
         const size_t n_vec8 = static_cast<size_t>(BH) * N * D / 8;
-        return static_cast<int>(launch_pdl(bwd_dq_convert_kernel, dim3(grid_for(n_vec8, 256, sms * 8)),
+        return static_cast<int>(launch_pdl(bwd_dq_convert_kernel, dim3(grid_for((n_vec8 + 3) / 4, 256, sms * 8)),
                                            dim3(256), 0, s, reinterpret_cast<const float4*>(dq_acc),
                                            static_cast<uint4*>(dq), N, Np, n_vec8, scale));
     } else {

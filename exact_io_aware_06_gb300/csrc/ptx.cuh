@@ -92,6 +92,22 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
     }
 }
 
+// mbar_wait for a thread whose waits are long and not on the critical path (a producer
+// that runs far ahead): between polls it sleeps for about `sleep_ns`, leaving the issue
+// slots of its sub-partition to the warps that compute.
+__device__ __forceinline__ bool mbar_wait_sleepy(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                                 const volatile int* abort, uint32_t sleep_ns) {
+    if (mbar_test_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+#pragma unroll 1
+    while (true) {
+        if (mbar_test_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+        __nanosleep(sleep_ns);
+    }
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
