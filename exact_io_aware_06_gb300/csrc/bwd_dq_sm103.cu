@@ -220,10 +220,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after();
             uint32_t rs[2][32], rp[2][32];
-            tmem_ld32(lb + C::kColS + 64 * half, rs[0]);
-            tmem_ld32(lb + C::kColS + 64 * half + 32, rs[1]);
-            tmem_ld32(lb + C::kColDP + 64 * half, rp[0]);
-            tmem_ld32(lb + C::kColDP + 64 * half + 32, rp[1]);
+            tmem_ld32_async(lb + C::kColS + 64 * half, rs[0]);
+            tmem_ld32_async(lb + C::kColS + 64 * half + 32, rs[1]);
+            tmem_ld32_async(lb + C::kColDP + 64 * half, rp[0]);
+            tmem_ld32_async(lb + C::kColDP + 64 * half + 32, rp[1]);
+            tmem_wait_ld();
+            reg_fence(rs[0]);
+            reg_fence(rs[1]);
+            reg_fence(rp[0]);
+            reg_fence(rp[1]);
             // causal diagonal block: query row r sees keys 0..r of the block
             const bool diag = args.causal && (j == qb);
             uint32_t pk[32];

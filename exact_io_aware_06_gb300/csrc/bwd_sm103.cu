@@ -512,8 +512,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                 uint32_t pk[32];  // P^T row (64 queries) as bf16 pairs
                 {
                     uint32_t r[2][32];
-                    tmem_ld32(lb + kColS + 64 * half, r[0]);
-                    tmem_ld32(lb + kColS + 64 * half + 32, r[1]);
+                    tmem_ld32_async(lb + kColS + 64 * half, r[0]);
+                    tmem_ld32_async(lb + kColS + 64 * half + 32, r[1]);
+                    tmem_wait_ld();
+                    reg_fence(r[0]);
+                    reg_fence(r[1]);
 #pragma unroll
                     for (int x2 = 0; x2 < 32; ++x2) {
                         const uint32_t* rr = r[x2 / 16];
@@ -548,10 +551,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                 if (!ok) break;
                 tc_fence_after();
                 uint8_t* dsrow = sb_ptr + kOffDS + b * kDSBytes + half * 16384 + key_in_blk * 128;
+                // dP^T of this half's 64 queries in two 32-column loads; the second load runs
+                // while the first 32 queries' dS is stored
+                uint32_t r[32];
+                tmem_ld32_async(lb + kColDP + 64 * half, r);
+                tmem_wait_ld();
+                reg_fence(r);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    uint32_t r[32];
-                    tmem_ld32(lb + kColDP + 64 * half + 32 * h, r);
                     uint32_t w[16];
 #pragma unroll
                     for (int x2 = 0; x2 < 16; ++x2) {
@@ -562,6 +569,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                         const float2 ds = __fmul2_rn(p, gg);
                         w[x2] = pack_bf16x2(ds.x, ds.y);
                     }
+                    if (h == 0) tmem_ld32_async(lb + kColDP + 64 * half + 32, r);
                     tmem_st16(lb + kColDP + 64 * half + 16 * h, w);
                     if constexpr (C::kFusedDQ) {
                         // queries 64*half + 32h .. +31 of this key row -> MN-major swizzled A tile
@@ -572,6 +580,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                             *reinterpret_cast<uint4*>(dsrow + gran * 16) =
                                 make_uint4(w[4 * g4], w[4 * g4 + 1], w[4 * g4 + 2], w[4 * g4 + 3]);
                         }
+                    }
+                    if (h == 0) {
+                        tmem_wait_ld();
+                        reg_fence(r);
                     }
                 }
                 tmem_st_wait();
@@ -679,8 +691,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                 if (!ok) break;
                 tc_fence_after();
                 uint32_t r[2][32];
-                tmem_ld32(lb + kColDQ + 64 * b, r[0]);
-                tmem_ld32(lb + kColDQ + 64 * b + 32, r[1]);
+                tmem_ld32_async(lb + kColDQ + 64 * b, r[0]);
+                tmem_ld32_async(lb + kColDQ + 64 * b + 32, r[1]);
+                tmem_wait_ld();
+                reg_fence(r[0]);
+                reg_fence(r[1]);
                 tc_fence_before();
                 mbar_arrive(smem_u32(&bars.dq_free[b]));
                 const uint32_t box0 = sb + kOffDS + b * kDSBytes + wq * 8192;  // two 4 KB boxes
