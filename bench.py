@@ -462,6 +462,22 @@ def cpu_sample(oracle, inputs, budget_s):
     return total_f, dt, desc
 
 
+def cpu_single_thread(oracle, inputs, seconds=2.0):
+    """The oracle on one host thread over the whole fp32 worked configuration (B=H=1,
+    N=128, d=64, non-causal), repeated for about `seconds`."""
+    import numpy as np
+    x = inputs.attention_inputs(1, 1, 128, 64, "f32")
+    q, k, v = (x[n].numpy().astype(np.float64) for n in "qkv")
+    fl, reps, t0 = 4 * 128 * 128 * 64, 0, time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        oracle.attn_fwd(q, k, v, 1 / 8.0, nthreads=1)
+        reps += 1
+    dt = time.perf_counter() - t0
+    return {"value": round(reps * fl / dt / 1e9, 3), "unit": "GFLOP/s", "cores": 1,
+            "sample": f"{reps} x fp32 forward B1 H1 N128 d64 (4.19 MFLOP each)",
+            "ms_per_call": round(1e3 * dt / reps, 3)}
+
+
 def bench_ours(args):
     import torch
     import torch.distributed as dist
@@ -634,7 +650,8 @@ def bench_ours(args):
         fl, dt, desc = cpu_sample(oracle, inputs, args.cpu_seconds)
         result["cpu_baseline"] = {"value": round(fl / dt / 1e12, 6), "unit": UNIT,
                                   "cores": oracle.max_threads(), "kind": "oracle",
-                                  "sample": desc, "seconds": round(dt, 2)}
+                                  "sample": desc, "seconds": round(dt, 2),
+                                  "single_thread_fp32_config": cpu_single_thread(oracle, inputs)}
     if world > 1:
         dist.destroy_process_group()
     if rank == 0:

@@ -740,100 +740,61 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 // -delta_i = -(dO_i . O_i) and -lse_i * log2(e) (rows past N: 0 and -inf, so
 // that recomputed P is exactly 0 there), dQ accumulator zeroed.  Both are stored
 // negated so the main kernel adds them with packed FMA/FADD.
-// D/8 lanes per row, each reading 16 bytes of O and of dO; a thread works on kRows
-// rows at once (all their loads in flight before the first use) and zeroes the same
-// rows of the accumulator, so the pass streams at close to the memory rate.
+// D/8 threads per row, each reading 16 bytes of O and dO.
 template <int D>
-__global__ void __launch_bounds__(256) bwd_prep_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dO,
-                                                       const float* __restrict__ lse, float* __restrict__ ws_delta,
-                                                       float* __restrict__ ws_lse2, float4* __restrict__ dq_acc,
-                                                       int BH, int N, int Np) {
+__global__ void bwd_prep_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dO,
+                                const float* __restrict__ lse, float* __restrict__ ws_delta,
+                                float* __restrict__ ws_lse2, float4* __restrict__ dq_acc, int BH,
+                                int N, int Np, size_t acc_vec4) {
     griddep_wait();               // O, dO may come from the kernel before this one
     griddep_launch_dependents();  // the main kernel may launch and set up meanwhile
-    constexpr int kT = D / 8;              // lanes per row (8 or 16): the shuffles stay in a warp
-    constexpr int kRowsPerWarp = 32 / kT;  // rows one warp covers per step
-    constexpr int kRows = 4;               // steps in flight per thread
-    const int lane = threadIdx.x & 31, part = lane % kT, sub = lane / kT;
-    const size_t warps = static_cast<size_t>(gridDim.x) * (blockDim.x / 32);
-    const size_t wid = static_cast<size_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
+    const size_t tid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const size_t nthreads = static_cast<size_t>(gridDim.x) * blockDim.x;
     const size_t rows = static_cast<size_t>(BH) * Np;
-    const size_t per_iter = static_cast<size_t>(kRowsPerWarp) * kRows;
-    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (size_t r0 = wid * per_iter; r0 < rows; r0 += warps * per_iter) {
-        uint4 a[kRows], b[kRows];
-        bool valid[kRows];
-#pragma unroll
-        for (int u = 0; u < kRows; ++u) {
-            const size_t r = r0 + static_cast<size_t>(u) * kRowsPerWarp + sub;
-            const int bh = static_cast<int>(r / Np), i = static_cast<int>(r % Np);
-            valid[u] = r < rows && i < N;
+    constexpr int kT = D / 8;  // threads per row (8 or 16): the shuffles stay inside a warp
+    for (size_t base = tid; base < rows * kT; base += nthreads) {
+        const size_t r = base / kT;
+        const int part = static_cast<int>(base % kT);
+        const int bh = static_cast<int>(r / Np), i = static_cast<int>(r % Np);
+        float sum = 0.f;
+        if (i < N) {
             const size_t src = (static_cast<size_t>(bh) * N + i) * kT + part;
-            a[u] = valid[u] ? o[src] : make_uint4(0u, 0u, 0u, 0u);
-            b[u] = valid[u] ? dO[src] : make_uint4(0u, 0u, 0u, 0u);
-        }
-        if (dq_acc != nullptr) {
-#pragma unroll
-            for (int u = 0; u < kRows; ++u) {
-                const size_t r = r0 + static_cast<size_t>(u) * kRowsPerWarp + sub;
-                if (r < rows) {  // D floats per row: D/4 float4, kT lanes -> 2 each
-                    dq_acc[r * (D / 4) + 2 * part] = z;
-                    dq_acc[r * (D / 4) + 2 * part + 1] = z;
-                }
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < kRows; ++u) {
-            const uint32_t av[4] = {a[u].x, a[u].y, a[u].z, a[u].w}, bv[4] = {b[u].x, b[u].y, b[u].z, b[u].w};
-            float sum = 0.f;
+            const uint4 a = o[src], b = dO[src];
+            const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
             for (int x = 0; x < 4; ++x) {
                 sum = fmaf(__uint_as_float(av[x] << 16), __uint_as_float(bv[x] << 16), sum);
                 sum = fmaf(__uint_as_float(av[x] & 0xFFFF0000u), __uint_as_float(bv[x] & 0xFFFF0000u), sum);
             }
-            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-            sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-            if (kT == 16) sum += __shfl_xor_sync(0xffffffffu, sum, 8);
-            const size_t r = r0 + static_cast<size_t>(u) * kRowsPerWarp + sub;
-            if (part == 0 && r < rows) {
-                const int bh = static_cast<int>(r / Np), i = static_cast<int>(r % Np);
-                ws_delta[r] = -sum;
-                ws_lse2[r] = valid[u] ? -lse[static_cast<size_t>(bh) * N + i] * kLog2e : -INFINITY;
-            }
+        }
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+        if (kT == 16) sum += __shfl_xor_sync(0xffffffffu, sum, 8);
+        if (part == 0) {
+            ws_delta[r] = -sum;
+            ws_lse2[r] = (i < N) ? -lse[static_cast<size_t>(bh) * N + i] * kLog2e : -INFINITY;
         }
     }
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (size_t x = tid; x < acc_vec4; x += nthreads) dq_acc[x] = z;
 }
 
-// dQ = bf16(scale * accumulator) for rows < N (d = 64); 8 elements per thread, kVecs
-// groups in flight per thread.
-__global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float4* __restrict__ acc, uint4* __restrict__ dq,
-                                                             int N, int Np, size_t n_vec8, float scale) {
+// dQ = bf16(scale * accumulator) for rows < N (d = 64); 8 elements per thread.
+__global__ void bwd_dq_convert_kernel(const float4* __restrict__ acc, uint4* __restrict__ dq,
+                                      int N, int Np, size_t n_vec8, float scale) {
     griddep_wait();  // launched while the main kernel may still run
-    constexpr int kVecs = 4;
+    const size_t tid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const size_t nthreads = static_cast<size_t>(gridDim.x) * blockDim.x;
     constexpr int kVecPerRow = 64 / 8;
-    for (size_t x0 = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; x0 < n_vec8;
-         x0 += nthreads * kVecs) {
-        float4 a[kVecs], b[kVecs];
-#pragma unroll
-        for (int u = 0; u < kVecs; ++u) {
-            const size_t x = x0 + u * nthreads;
-            if (x < n_vec8) {
-                const size_t row = x / kVecPerRow;  // row in [BH][N]
-                const int part = static_cast<int>(x % kVecPerRow);
-                const size_t bh = row / N, i = row % N;
-                const size_t src = ((bh * Np + i) * kVecPerRow + part) * 2;
-                a[u] = acc[src];
-                b[u] = acc[src + 1];
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < kVecs; ++u) {
-            const size_t x = x0 + u * nthreads;
-            if (x < n_vec8)
-                dq[x] = make_uint4(pack_bf16x2(a[u].x * scale, a[u].y * scale), pack_bf16x2(a[u].z * scale, a[u].w * scale),
-                                   pack_bf16x2(b[u].x * scale, b[u].y * scale), pack_bf16x2(b[u].z * scale, b[u].w * scale));
-        }
+    for (size_t x = tid; x < n_vec8; x += nthreads) {
+        const size_t row = x / kVecPerRow;  // row in [BH][N]
+        const int part = static_cast<int>(x % kVecPerRow);
+        const size_t bh = row / N, i = row % N;
+        const size_t src = ((bh * Np + i) * kVecPerRow + part) * 2;
+        const float4 a = acc[src], b = acc[src + 1];
+        dq[x] = make_uint4(pack_bf16x2(a.x * scale, a.y * scale), pack_bf16x2(a.z * scale, a.w * scale),
+                           pack_bf16x2(b.x * scale, b.y * scale), pack_bf16x2(b.z * scale, b.w * scale));
     }
 }
 
@@ -869,11 +830,10 @@ int launch_bwd_impl(const void* q, const void* k, const void* v, const void* o, 
     int sms = 152, dev = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    // prep: a warp covers 32/(D/8) rows per step and 4 steps at once
-    const size_t prep_warps = (static_cast<size_t>(BH) * Np + (32 / (D / 8)) * 4 - 1) / ((32 / (D / 8)) * 4);
-    cudaError_t e = launch_pdl(bwd_prep_kernel<D>, dim3(grid_for(prep_warps * 32, 256, sms * 8)), dim3(256), 0, s,
-                               static_cast<const uint4*>(o), static_cast<const uint4*>(dO), lse, ws_delta, ws_lse2,
-                               reinterpret_cast<float4*>(dq_acc), BH, N, Np);
+    const size_t acc_vec4 = C::kFusedDQ ? static_cast<size_t>(BH) * Np * D / 4 : 0;
+    cudaError_t e = launch_pdl(bwd_prep_kernel<D>, dim3(grid_for(static_cast<size_t>(BH) * Np * (D / 8), 256, sms * 8)),
+                               dim3(256), 0, s, static_cast<const uint4*>(o), static_cast<const uint4*>(dO), lse,
+                               ws_delta, ws_lse2, reinterpret_cast<float4*>(dq_acc), BH, N, Np, acc_vec4);
     if (e != cudaSuccess) return static_cast<int>(e);
 
     CUtensorMap tq, tk, tv, tdo;
@@ -932,7 +892,7 @@ int launch_bwd_impl(const void* q, const void* k, const void* v, const void* o, 
 
     if constexpr (C::kFusedDQ) {
         const size_t n_vec8 = static_cast<size_t>(BH) * N * D / 8;
-        return static_cast<int>(launch_pdl(bwd_dq_convert_kernel, dim3(grid_for((n_vec8 + 3) / 4, 256, sms * 8)),
+        return static_cast<int>(launch_pdl(bwd_dq_convert_kernel, dim3(grid_for(n_vec8, 256, sms * 8)),
                                            dim3(256), 0, s, reinterpret_cast<const float4*>(dq_acc),
                                            static_cast<uint4*>(dq), N, Np, n_vec8, scale));
     } else {
