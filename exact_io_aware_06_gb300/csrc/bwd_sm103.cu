@@ -141,7 +141,7 @@ struct Bars {
     uint64_t ds_empty[2];
     uint64_t dq_full[2], dq_free[2];
     uint64_t all_done;
-    uint64_t epi_staged, epi_free;  // d = 64: an item's dV, dK staged / stored from smem
+    uint64_t epi_staged;  // d = 64: an item's dV, dK staged in shared memory
     uint64_t drain, drain2;
 };
 
@@ -236,7 +236,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         mbar_init(smem_u32(&bars.ds_full[1]), 256);
         mbar_init(smem_u32(&bars.all_done), 1);
         mbar_init(smem_u32(&bars.epi_staged), 256);
-        mbar_init(smem_u32(&bars.epi_free), 1);
         mbar_init(smem_u32(&bars.drain), 1);
         mbar_init(smem_u32(&bars.drain2), 1);
         fence_barrier_init();
@@ -424,7 +423,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                     for (int kk = 0; kk < kBlk / 16; ++kk)
                         mma_bf16_ts(tmem + kColDK, tmem + kColDP + 64 * (kk >> 2) + 8 * (kk & 3),
                                     sdesc_sw128(sQ + 2048 * kk, 16384, 1024), kIdescTS, (i > 0) || (kk > 0));
-                    mma_commit(smem_u32(&bars.q_empty[s]));  // Q_i, dO_i, lse_i, delta_i consumed
+                    // Q_i, dO_i, lse_i, delta_i consumed.  At d = 64 the item's last block hands
+                    // its ring stage to the epilogue instead, which stages dV and dK in it and
+                    // releases it once the TMA stores have read them.
+                    if constexpr (more || !C::kFusedDQ) mma_commit(smem_u32(&bars.q_empty[s]));
                     if constexpr (more) {
                         issue_dp(s1);
                         if constexpr (last2) mma_commit(smem_u32(&bars.v_empty));  // V's last dP
@@ -492,6 +494,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         const int key_in_blk = wq * 32 + lane;
         const uint32_t lb = tmem + (static_cast<uint32_t>(wq * 32) << 16);
         const float2 c2 = make_float2(args.c_log2, args.c_log2);
+        int epi_stage = -1;  // warp 4 lane 0: the ring stage whose dV/dK stores are in flight
         bool ok = true;
         int g = 0, kc = 0;
         for (int k = 0, x = item_x(0); x < n_items && ok; x = item_x(++k), ++kc) {
@@ -543,10 +546,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                 ok = mbar_wait(smem_u32(&bars.dp_full), gi & 1, lim, &abort_flag);
                 if (C::kFusedDQ && ok && gi >= 2)
                     ok = mbar_wait(smem_u32(&bars.ds_empty[b]), ((gi >> 1) & 1) ^ 1, lim, &abort_flag);
-                // the previous item's dV, dK were staged in this buffer: their TMA stores
-                // must have read it
-                if (C::kFusedDQ && ok && i == 0 && kc > 0)
-                    ok = mbar_wait(smem_u32(&bars.epi_free), (kc - 1) & 1, lim, &abort_flag);
+                // the previous item's dV, dK stores: once they have read their ring stage,
+                // hand it back to the producer (normally long done by now)
+                if (C::kFusedDQ && warp == 4 && lane == 0 && epi_stage >= 0) {
+                    bulk_wait_read_all();
+                    mbar_arrive(smem_u32(&bars.q_empty[epi_stage]));
+                    epi_stage = -1;
+                }
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();
@@ -593,18 +599,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             }
             if (!ok) break;
             if constexpr (C::kFusedDQ) {
-                // epilogue (d = 64): warps 4-7 stage dV, warps 8-11 dK (times scale) in the dS
-                // buffer that the next item's first block will use -- free once the drain has
-                // reduced the dQ staged there two blocks ago -- as 128-byte swizzled
-                // 128 x 64 boxes; one thread writes them with TMA stores of whole lines.
-                const int gn = g + I.n_it, bn = gn & 1;
+                // epilogue (d = 64): warps 4-7 stage dV, warps 8-11 dK (times scale) as
+                // 128-byte swizzled 128 x 64 boxes in the Q/dO ring stage of the item's last
+                // block (dV over its dO tile, dK over its Q tile), free once that block's dV
+                // and dK have completed (all_done); one thread writes them with TMA stores of
+                // whole lines and hands the stage back to the producer once the stores have
+                // read it, at its next dS phase, so the stores' latency stays off the next
+                // item's first blocks.
+                const int sl = (g + I.n_it - 1) % kQStages;
                 ok = mbar_wait(smem_u32(&bars.all_done), kc & 1, lim, &abort_flag);
-                if (ok && gn >= 2)
-                    ok = mbar_wait(smem_u32(&bars.ds_empty[bn]), ((gn >> 1) & 1) ^ 1, lim, &abort_flag);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t box = sb + kOffDS + bn * kDSBytes + half * 16384;
+                const uint32_t box = sb + (half ? kOffQ : kOffDO) + sl * kTile;
                 const float sc = half ? args.scale : 1.0f;
                 const uint32_t col = half ? kColDK : kColDV;
 #pragma unroll
@@ -625,11 +632,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                 mbar_arrive(smem_u32(&bars.epi_staged));
                 if (warp == 4 && lane == 0) {
                     if (mbar_wait(smem_u32(&bars.epi_staged), kc & 1, lim, &abort_flag)) {
-                        tma_store_3d(&tm_dv, box - half * 16384, 0, I.kvb * kBlk, I.bh);
-                        tma_store_3d(&tm_dk, box - half * 16384 + 16384, 0, I.kvb * kBlk, I.bh);
+                        tma_store_3d(&tm_dv, sb + kOffDO + sl * kTile, 0, I.kvb * kBlk, I.bh);
+                        tma_store_3d(&tm_dk, sb + kOffQ + sl * kTile, 0, I.kvb * kBlk, I.bh);
                         bulk_commit_group();
-                        bulk_wait_read_all();
-                        mbar_arrive(smem_u32(&bars.epi_free));
+                        epi_stage = sl;
                     } else {
                         ok = false;
                     }
