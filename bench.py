@@ -17,10 +17,11 @@ inputs copied in and outputs copied out inside the timed region, each part's cop
 on their own streams so that they overlap the other parts' compute.
 
 ``extras`` times the variant rows alone, after the step and outside ``value``
-(10 launches each after 3 warm-ups): backward at d=128 and causal, FP8 causal
+(the median of 20 launches each, after 3 warm-ups): backward at d=128 and causal, FP8 causal
 and per-head and per-128-row-block scale factors, grouped-query forward/backward (32 query heads on 8 K/V heads),
-and the forward sharded over 4 key blocks of the sequence plus the lse merge
-(with the merge kernel's achieved HBM bandwidth).
+and the forward sharded over 4 key blocks of the sequence (the shards on 4 streams side
+by side, as they would run on 4 GPUs) plus the lse merge (with the merge kernel's achieved
+HBM bandwidth).
 
 ``--impl reference`` times the fp64 CPU oracle instead (the comparison arm) on a
 bounded sample of the same workload, on this machine's host cores.
@@ -340,11 +341,20 @@ def make_extra(torch, fa, inputs, ex, dev, stream):
     o_p = torch.empty((S, B, H, N, d), dtype=torch.float32, device=dev)
     l_p = torch.empty((S, B, H, N), dtype=torch.float32, device=dev)
     mid = torch.cuda.Event(enable_timing=True)
+    # the shards are independent (on several GPUs they would run side by side): each runs
+    # on its own stream after the launch stream's prior work, and the merge waits for all
+    side = [torch.cuda.Stream(device=dev) for _ in range(S)]
+    start, done = torch.cuda.Event(), [torch.cuda.Event() for _ in range(S)]
 
     def run():
+        start.record(stream)
         for t in range(S):
+            side[t].wait_event(start)
             fa.fa_fwd_kv_shard(q, ks[t], vs[t], o_p[t], l_p[t], s, causal, 0, t * n,
-                               fa.FA_BF16, stream)
+                               fa.FA_BF16, side[t])
+            done[t].record(side[t])
+        for t in range(S):
+            stream.wait_event(done[t])
         mid.record(stream)
         fa.fa_lse_merge(o_p, l_p, o, lse, fa.FA_BF16, stream)
     # algorithmic bytes of the merge: every part's lse, the O rows of the parts whose
@@ -356,7 +366,7 @@ def make_extra(torch, fa, inputs, ex, dev, stream):
     return run, f_fwd, {"mid": mid, "merge_bytes": merge_bytes, "launches": S + 1}
 
 
-def time_extras(torch, fa, inputs, dev, stream, pk, iters=10, warmup=3):
+def time_extras(torch, fa, inputs, dev, stream, pk, iters=20, warmup=3):
     out = {}
     for ex in EXTRAS:
         name, what = ex[0], ex[1]
@@ -377,15 +387,15 @@ def time_extras(torch, fa, inputs, dev, stream, pk, iters=10, warmup=3):
         st = fa.fa_last_device_error()
         if st != 0:
             raise RuntimeError(f"{name}: device status {fa.fa_status_string(st)}")
-        mean = sum(ms) / len(ms)
-        tf = fl / (mean * 1e-3) / 1e12
-        rec = {"ms": round(mean, 4), "tflops": round(tf, 1), "flop": fl}
+        med = statistics.median(ms)
+        tf = fl / (med * 1e-3) / 1e12
+        rec = {"ms": round(med, 4), "mean_ms": round(sum(ms) / len(ms), 4), "tflops": round(tf, 1), "flop": fl}
         if what.startswith("fwd8"):
             rec["dtype"] = "e4m3"
         else:
             rec["pct_of_peak"] = round(100 * tf / pk["bf16"], 1)
         if sub is not None:
-            mm = sum(merge_ms) / len(merge_ms)
+            mm = statistics.median(merge_ms)
             gbs = sub["merge_bytes"] / (mm * 1e-3) / 1e9
             rec["merge"] = {"kernel": "lse_merge_kernel<128,bf16>", "bound": "hbm", "ms": round(mm, 4),
                             "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
