@@ -62,3 +62,41 @@ def test_max_over_ranks_with_gloo_world_2():
 def test_single_process_reduction_is_identity():
     b = load_bench()
     assert b.max_over_ranks([3.0, 4.0]) == [3.0, 4.0]
+
+
+def test_roofline_record_fraction_and_fields():
+    b = load_bench()
+    rec = b.roofline_record("k", 967.05, 1934.1, "measured", "no-such-record", 1000)
+    assert rec["frac"] == pytest.approx(0.5)
+    assert rec["bound"] == "tensor" and rec["unit"] == "TFLOP/s"
+    assert rec["traffic"] is None  # no capture recorded under that key
+    assert rec["algorithmic_bytes"] == 1000
+
+
+def test_recorded_traffic_follows_its_sources(tmp_path, monkeypatch):
+    # a record is used only while the sources it was captured on are unchanged
+    import hashlib
+    import json
+    b = load_bench()
+    src = tmp_path / "k.cu"
+    src.write_text("kernel v1")
+    (tmp_path / "profiles").mkdir()
+    rec = {"k": {"source_files": ["k.cu"], "traffic_bytes_per_launch": 123,
+                 "source_sha256": hashlib.sha256(b"kernel v1").hexdigest()}}
+    (tmp_path / "profiles" / "roofline_traffic.json").write_text(json.dumps(rec))
+    monkeypatch.setattr(b, "ROOT", str(tmp_path))
+    assert b.recorded_traffic("k") == 123
+    assert b.recorded_traffic("other") is None
+    src.write_text("kernel v2")
+    assert b.recorded_traffic("k") is None
+
+
+def test_committed_traffic_records_name_existing_sources():
+    import json
+    path = os.path.join(ROOT, "profiles", "roofline_traffic.json")
+    recs = json.load(open(path))
+    assert {"fwd_bf16_b1h32n16384d128", "bwd_bf16_b4h16n2048d64", "fwd_e4m3_b4h16n4096d128"} <= set(recs)
+    for rec in recs.values():
+        for f in rec["source_files"]:
+            assert os.path.exists(os.path.join(ROOT, f)), f
+        assert rec["traffic_bytes_per_launch"] == rec["dram_bytes_read"] + rec["dram_bytes_write"]
