@@ -21,12 +21,14 @@
 // bwd_main layout (d = 64), 16 warps:
 //   warp 0      TMA producer: Q_i, dO_i, lse_i, delta_i in a 3-stage ring that runs
 //               across item boundaries
-//   warp 3      TMA producer: K_j (two buffers: the next item's K loads while this item
-//               runs) and V_j (reloaded as soon as the item's last dP has read it)
 //   warp 1      MMA issuer (dV, S, dK, dP) + TMEM owner
 //   warp 2      second MMA issuer: dQ (d = 64 only)
+//   warp 3      TMA producer: K_j (two buffers: the next item's K loads while this item
+//               runs) and V_j (reloaded as soon as the item's last dP has read it)
 //   warps 4-7   P/dS for query columns 0-63 of block i   (thread = key row)
-//   warps 8-11  P/dS for query columns 64-127
+//   warps 8-11  P/dS for query columns 64-127; at an item's end these 8 warps stage dV
+//               and dK in the ring stage of the item's last block and warp 4 writes
+//               them with TMA stores
 //   warps 12-15 drain dQ_i from TMEM into the fp32 accumulator: each warp stages its
 //               32 rows in the dS buffer that dQ_i has just consumed (128-byte
 //               swizzled boxes) and adds them with TMA bulk tensor reductions
