@@ -177,3 +177,35 @@ def test_sharded_b1_h32_n16384_d128_causal_sampled_rows():
                                               f64(x["v"][0, h]), rows, s, True)
         assert max_err(o[0, h, rows], o_ref) <= TOL_BF16_O
         assert max_err(lse[0, h, rows], lse_ref) <= TOL_LSE_BF16
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_key_shards_on_side_streams_merge_to_full_forward(causal):
+    # The shards are independent: launched on four streams side by side (as they would run
+    # on four GPUs) after the launch stream's work, then merged on the launch stream once
+    # all four have finished.  The result is the forward over the whole sequence.
+    B, H, N, d, S = 1, 4, 2048, 128, 4
+    n = N // S
+    q, k, v = (bf16((B, H, N, d), 42 + i).cuda() for i in range(3))
+    s = scale_for(d)
+    ks = [k[:, :, t * n:(t + 1) * n].contiguous() for t in range(S)]
+    vs = [v[:, :, t * n:(t + 1) * n].contiguous() for t in range(S)]
+    o_p = torch.empty((S, B, H, N, d), dtype=torch.float32, device="cuda")
+    l_p = torch.empty((S, B, H, N), dtype=torch.float32, device="cuda")
+    o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    main = torch.cuda.current_stream()
+    side = [torch.cuda.Stream() for _ in range(S)]
+    start, done = torch.cuda.Event(), [torch.cuda.Event() for _ in range(S)]
+    start.record(main)
+    for t in range(S):
+        side[t].wait_event(start)
+        fa.fa_fwd_kv_shard(q, ks[t], vs[t], o_p[t], l_p[t], s, causal, 0, t * n, fa.FA_BF16, side[t])
+        done[t].record(side[t])
+    for t in range(S):
+        main.wait_event(done[t])
+    fa.fa_lse_merge(o_p, l_p, o, lse, fa.FA_BF16, main)
+    check_status()
+    o_ref, lse_ref = oracle.attn_fwd(f64(q), f64(k), f64(v), s, causal)
+    assert max_err(f64(o), o_ref) <= TOL_BF16_O
+    assert max_err(f64(lse), lse_ref) <= TOL_LSE_BF16
