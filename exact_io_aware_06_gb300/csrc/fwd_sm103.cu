@@ -315,38 +315,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             const uint32_t sQ0 = smem_base + C::kOffQ, sQ1 = sQ0 + C::kTileBytes;
             bool ok = mbar_wait(smem_u32(&bars.q_full), 0, lim, &abort_flag);
-            auto issue_s = [&](uint32_t sQ, int s, uint32_t col) {
-                const uint32_t sK = smem_base + C::kOffK + s * C::kTileBytes;
+            // Operand descriptors: the low words of Q_t and of stage 0 of the K and V rings
+            // are computed once; each MMA adds its K step's offset (see sdesc_sw128_lo).
+            constexpr uint32_t kDescHi = sdesc_sw128_hi(1024);
+            const uint32_t q_lo0 = sdesc_sw128_lo(sQ0, 16), q_lo1 = sdesc_sw128_lo(sQ1, 16);
+            const uint32_t k_lo = sdesc_sw128_lo(smem_base + C::kOffK, 16);
+            const uint32_t v_lo = sdesc_sw128_lo(smem_base + C::kOffV, C::kChunkBytes);
+            auto issue_s = [&](uint32_t q_lo, int s, uint32_t col) {
+                const uint32_t kl = k_lo + s * (C::kTileBytes >> 4);
 #pragma unroll
                 for (int kk = 0; kk < D / C::kKStep; ++kk) {
-                    const uint32_t off = (kk * C::kStepBytes) / 128 * C::kChunkBytes +
-                                         (kk * C::kStepBytes) % 128;
-                    const uint64_t da = sdesc_sw128(sQ + off, 16, 1024);
-                    const uint64_t db = sdesc_sw128(sK + off, 16, 1024);
-                    if (FP8)
-                        mma_e4m3_ss(tmem + col, da, db, C::kIdescS, kk > 0);
+                    const uint32_t off16 = ((kk * C::kStepBytes) / 128 * C::kChunkBytes +
+                                            (kk * C::kStepBytes) % 128) >> 4;
+                    if (kk == 0)
+                        mma_ss_w<FP8, -1>(tmem + col, q_lo, kl, kDescHi, C::kIdescS, 0u);
                     else
-                        mma_bf16_ss(tmem + col, da, db, C::kIdescS, kk > 0);
+                        mma_ss_w<FP8, 1>(tmem + col, q_lo + off16, kl + off16, kDescHi, C::kIdescS);
                 }
             };
             auto issue_pv = [&](uint32_t colP, int s, uint32_t colO, bool acc) {
-                const uint32_t sV = smem_base + C::kOffV + s * C::kTileBytes;
+                const uint32_t vl = v_lo + s * (C::kTileBytes >> 4);
 #pragma unroll
                 for (int kk = 0; kk < kBN / C::kKStep; ++kk) {
-                    const uint64_t db = sdesc_sw128(sV + kk * C::kKStep * 128, C::kChunkBytes, 1024);
-                    if (FP8)
-                        mma_e4m3_ts(tmem + colO, tmem + colP + kk * 8, db, C::kIdescO, acc || kk > 0);
+                    if (kk == 0)
+                        mma_ts_w<FP8, -1>(tmem + colO, tmem + colP, vl, kDescHi, C::kIdescO, acc ? 1u : 0u);
                     else
-                        mma_bf16_ts(tmem + colO, tmem + colP + kk * 8, db, C::kIdescO, acc || kk > 0);
+                        mma_ts_w<FP8, 1>(tmem + colO, tmem + colP + kk * 8, vl + ((kk * C::kKStep * 128) >> 4),
+                                         kDescHi, C::kIdescO);
                 }
             };
             if (SHARD && n_kv == 0) ok = false;  // nothing to multiply; not an error
             if (ok) ok = mbar_wait(smem_u32(&bars.k_full[0]), 0, lim, &abort_flag);
             if (ok) {
                 tc_fence_after();
-                issue_s(sQ0, 0, C::kColS0);
+                issue_s(q_lo0, 0, C::kColS0);
                 mma_commit(smem_u32(&bars.s_full[0]));
-                issue_s(sQ1, 0, C::kColS1);
+                issue_s(q_lo1, 0, C::kColS1);
                 mma_commit(smem_u32(&bars.s_full[1]));
                 mma_commit(smem_u32(&bars.k_empty[0]));
             }
@@ -365,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = mbar_wait(smem_u32(&bars.k_full[s1]), ph1, lim, &abort_flag);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_s(sQ0, s1, C::kColS0);
+                    issue_s(q_lo0, s1, C::kColS0);
                     mma_commit(smem_u32(&bars.s_full[0]));
                 } else {
                     mma_commit(smem_u32(&bars.o_done[0]));
@@ -376,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 issue_pv(C::kColS1, s, C::kColO1, j > 0);
                 mma_commit(smem_u32(&bars.v_empty[s]));
                 if (more) {
-                    issue_s(sQ1, s1, C::kColS1);
+                    issue_s(q_lo1, s1, C::kColS1);
                     mma_commit(smem_u32(&bars.s_full[1]));
                     mma_commit(smem_u32(&bars.k_empty[s1]));
                 } else {

@@ -227,6 +227,84 @@ __device__ __forceinline__ void mma_e4m3_ts(uint32_t d_tmem, uint32_t a_tmem, ui
         : "memory");
 }
 
+// sdesc_sw128 split into its two 32-bit words: the low word holds the start address and
+// the leading byte offset, the high word the stride byte offset and the fixed fields.  An
+// issue loop computes an operand's low word once and adds (byte offset / 16) per K step:
+// the 14-bit address field cannot overflow, shared addresses being below 2^18.  Issuing
+// MMAs back to back then costs the issuing thread one add per operand instead of a
+// 64-bit descriptor build.
+__device__ __forceinline__ uint32_t sdesc_sw128_lo(uint32_t saddr, uint32_t lbo) {
+    return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+__host__ __device__ constexpr uint32_t sdesc_sw128_hi(uint32_t sbo) {
+    return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+}
+
+// D[tmem] (+)= A[smem] * B[smem] and D[tmem] (+)= A[tmem] * B[smem] with the descriptors
+// as (low word, shared high word).  ACC < 0: accumulate iff `accumulate` != 0;
+// ACC = 1: accumulate, without a predicate to compute.  kind::f16 (bf16) or, for FP8,
+// kind::f8f6f4 (E4M3).
+template <bool FP8, int ACC>
+__device__ __forceinline__ void mma_ss_w(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi,
+                                         uint32_t idesc, uint32_t accumulate = 1) {
+    if constexpr (ACC == 1 && !FP8)
+        asm volatile(
+            "{\n\t.reg .b64 da, db;\n\tmov.b64 da, {%1, %3};\n\tmov.b64 db, {%2, %3};\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, 1;\n\t}" ::"r"(d_tmem),
+            "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc)
+            : "memory");
+    else if constexpr (ACC == 1)
+        asm volatile(
+            "{\n\t.reg .b64 da, db;\n\tmov.b64 da, {%1, %3};\n\tmov.b64 db, {%2, %3};\n\t"
+            "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %4, 1;\n\t}" ::"r"(d_tmem),
+            "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc)
+            : "memory");
+    else if constexpr (!FP8)
+        asm volatile(
+            "{\n\t.reg .b64 da, db;\n\t.reg .pred p;\n\tmov.b64 da, {%1, %3};\n\t"
+            "mov.b64 db, {%2, %3};\n\tsetp.ne.b32 p, %5, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p;\n\t}" ::"r"(d_tmem),
+            "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .b64 da, db;\n\t.reg .pred p;\n\tmov.b64 da, {%1, %3};\n\t"
+            "mov.b64 db, {%2, %3};\n\tsetp.ne.b32 p, %5, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %4, p;\n\t}" ::"r"(d_tmem),
+            "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate)
+            : "memory");
+}
+template <bool FP8, int ACC>
+__device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t hi,
+                                         uint32_t idesc, uint32_t accumulate = 1) {
+    if constexpr (ACC == 1 && !FP8)
+        asm volatile(
+            "{\n\t.reg .b64 db;\n\tmov.b64 db, {%2, %3};\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, 1;\n\t}" ::"r"(d_tmem),
+            "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc)
+            : "memory");
+    else if constexpr (ACC == 1)
+        asm volatile(
+            "{\n\t.reg .b64 db;\n\tmov.b64 db, {%2, %3};\n\t"
+            "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], db, %4, 1;\n\t}" ::"r"(d_tmem),
+            "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc)
+            : "memory");
+    else if constexpr (!FP8)
+        asm volatile(
+            "{\n\t.reg .b64 db;\n\t.reg .pred p;\n\tmov.b64 db, {%2, %3};\n\t"
+            "setp.ne.b32 p, %5, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+            "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .b64 db;\n\t.reg .pred p;\n\tmov.b64 db, {%2, %3};\n\t"
+            "setp.ne.b32 p, %5, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+            "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate)
+            : "memory");
+}
+
 // Arrive (once) on `bar` when every tcgen05 operation this thread issued so far
 // has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
