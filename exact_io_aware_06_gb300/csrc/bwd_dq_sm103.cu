@@ -152,21 +152,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ================================================================ MMA issuer
         if (lane == 0) {
-            const uint32_t sQ = sb + C::kOffQ, sDO = sb + C::kOffDO;
+            // Operand descriptors as low words built once (see sdesc_sw128_lo): K-major
+            // (leading byte offset 16) for S and dP, MN-major (16384) for K in dQ; each MMA
+            // adds its K step's offset / 16.
+            constexpr uint32_t kDescHi = sdesc_sw128_hi(1024);
+            constexpr uint32_t kStage16 = C::kTile >> 4;
+            const uint32_t q_lo = sdesc_sw128_lo(sb + C::kOffQ, 16), do_lo = sdesc_sw128_lo(sb + C::kOffDO, 16);
+            const uint32_t k_lo = sdesc_sw128_lo(sb + C::kOffK, 16), v_lo = sdesc_sw128_lo(sb + C::kOffV, 16);
+            const uint32_t k_mn = sdesc_sw128_lo(sb + C::kOffK, 16384);
             // S = Q K_j^T and dP = dO V_j^T (both operands K-major along d)
             auto issue_sp = [&](int s) {
-                const uint32_t sK = sb + C::kOffK + s * C::kTile, sV = sb + C::kOffV + s * C::kTile;
+                const uint32_t kl = k_lo + s * kStage16, vl = v_lo + s * kStage16;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    mma_bf16_ss(tmem + C::kColS, sdesc_sw128(sQ + off, 16, 1024),
-                                sdesc_sw128(sK + off, 16, 1024), C::kIdescSS, kk > 0);
+                    const uint32_t off16 = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                    if (kk == 0)
+                        mma_ss_w<false, -1>(tmem + C::kColS, q_lo, kl, kDescHi, C::kIdescSS, 0u);
+                    else
+                        mma_ss_w<false, 1>(tmem + C::kColS, q_lo + off16, kl + off16, kDescHi, C::kIdescSS);
                 }
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    mma_bf16_ss(tmem + C::kColDP, sdesc_sw128(sDO + off, 16, 1024),
-                                sdesc_sw128(sV + off, 16, 1024), C::kIdescSS, kk > 0);
+                    const uint32_t off16 = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                    if (kk == 0)
+                        mma_ss_w<false, -1>(tmem + C::kColDP, do_lo, vl, kDescHi, C::kIdescSS, 0u);
+                    else
+                        mma_ss_w<false, 1>(tmem + C::kColDP, do_lo + off16, vl + off16, kDescHi, C::kIdescSS);
                 }
                 mma_commit(smem_u32(&bars.sp_full));
             };
@@ -182,11 +193,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 tc_fence_after();
                 // dQ += dS_j K_j: A = dS from TMEM (queries x keys), B = K_j MN-major (d contiguous)
-                const uint32_t sK = sb + C::kOffK + s * C::kTile;
+                const uint32_t km = k_mn + s * kStage16;
 #pragma unroll
-                for (int kk = 0; kk < kBlk / 16; ++kk)
-                    mma_bf16_ts(tmem + C::kColDQ, tmem + C::kColS + 64 * (kk >> 2) + 8 * (kk & 3),
-                                sdesc_sw128(sK + 2048 * kk, 16384, 1024), C::kIdescDQ, (j > 0) || (kk > 0));
+                for (int kk = 0; kk < kBlk / 16; ++kk) {
+                    if (kk == 0)
+                        mma_ts_w<false, -1>(tmem + C::kColDQ, tmem + C::kColS, km, kDescHi, C::kIdescDQ, j > 0 ? 1u : 0u);
+                    else
+                        mma_ts_w<false, 1>(tmem + C::kColDQ, tmem + C::kColS + 64 * (kk >> 2) + 8 * (kk & 3),
+                                           km + 128 * kk, kDescHi, C::kIdescDQ);
+                }
                 mma_commit(smem_u32(&bars.kv_empty[s]));  // K_j and V_j consumed
                 if (j + 1 < n_kv) {
                     const int s1 = (j + 1) % kStages;

@@ -341,25 +341,37 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     } else if (warp == 1) {
         // ================================================================ MMA issuer
         if (lane == 0) {
-            const uint32_t sV = sb + kOffV;
-            uint32_t sK = sb + kOffK;  // this item's K buffer
+            // Operand descriptors as low words built once (see sdesc_sw128_lo): K-major
+            // (leading byte offset 16) for S^T and dP^T, MN-major (16384) for dV and dK.
+            // A stage's word is stage 0's plus s * kTile / 16; each MMA adds its K step's
+            // offset / 16.
+            constexpr uint32_t kDescHi = sdesc_sw128_hi(1024);
+            constexpr uint32_t kStage16 = kTile >> 4;
+            const uint32_t v_lo = sdesc_sw128_lo(sb + kOffV, 16);
+            const uint32_t q_lo = sdesc_sw128_lo(sb + kOffQ, 16), q_mn = sdesc_sw128_lo(sb + kOffQ, 16384);
+            const uint32_t do_lo = sdesc_sw128_lo(sb + kOffDO, 16), do_mn = sdesc_sw128_lo(sb + kOffDO, 16384);
+            uint32_t k_lo = sdesc_sw128_lo(sb + kOffK, 16);  // this item's K buffer
             auto issue_s = [&](int s) {  // S^T = K_j Q^T into columns 0-127
-                const uint32_t sQ = sb + kOffQ + s * kTile;
+                const uint32_t ql = q_lo + s * kStage16;
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    mma_bf16_ss(tmem + kColS, sdesc_sw128(sK + off, 16, 1024),
-                                sdesc_sw128(sQ + off, 16, 1024), kIdescSS, kk > 0);
+                    const uint32_t off16 = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                    if (kk == 0)
+                        mma_ss_w<false, -1>(tmem + kColS, k_lo, ql, kDescHi, kIdescSS, 0u);
+                    else
+                        mma_ss_w<false, 1>(tmem + kColS, k_lo + off16, ql + off16, kDescHi, kIdescSS);
                 }
                 mma_commit(smem_u32(&bars.s_full));
             };
             auto issue_dp = [&](int s) {  // dP^T = V_j dO^T into columns 128-255
-                const uint32_t sDO = sb + kOffDO + s * kTile;
+                const uint32_t dl = do_lo + s * kStage16;
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    mma_bf16_ss(tmem + kColDP, sdesc_sw128(sV + off, 16, 1024),
-                                sdesc_sw128(sDO + off, 16, 1024), kIdescSS, kk > 0);
+                    const uint32_t off16 = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                    if (kk == 0)
+                        mma_ss_w<false, -1>(tmem + kColDP, v_lo, dl, kDescHi, kIdescSS, 0u);
+                    else
+                        mma_ss_w<false, 1>(tmem + kColDP, v_lo + off16, dl + off16, kDescHi, kIdescSS);
                 }
                 mma_commit(smem_u32(&bars.dp_full));
             };
@@ -368,7 +380,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             for (int k = 0, x = item_x(0); x < n_items && ok; x = item_x(++k), ++kc) {
                 const Item I = item_at(x);
                 const int kb = kc % C::kKBufs;
-                sK = sb + kOffK + kb * kTile;
+                k_lo = sdesc_sw128_lo(sb + kOffK + kb * kTile, 16);
                 // the item's first scores; S and dP of the previous item's last block were
                 // read by its dV and dK, issued before these by this thread.  K and V are
                 // released after their last readers: K after the item's last S (and, d = 64,
@@ -395,7 +407,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                     const int gi = g + i;
                     const int s = gi % kQStages;
                     const int s1 = (gi + 1) % kQStages;
-                    const uint32_t sQ = sb + kOffQ + s * kTile, sDO = sb + kOffDO + s * kTile;
+                    const uint32_t qm = q_mn + s * kStage16, dm = do_mn + s * kStage16;
                     // The loads of block i+1 (ready blocks ahead) are checked together with
                     // P_i: every wait of an issuing thread can leave the tensor pipe idle.
                     // P of an item's first block is computed after the P/dS warps have read
@@ -407,9 +419,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                     tc_fence_after();
                     // dV += P^T dO_i
 #pragma unroll
-                    for (int kk = 0; kk < kBlk / 16; ++kk)
-                        mma_bf16_ts(tmem + kColDV, tmem + kColS + 64 * (kk >> 2) + 8 * (kk & 3),
-                                    sdesc_sw128(sDO + 2048 * kk, 16384, 1024), kIdescTS, (i > 0) || (kk > 0));
+                    for (int kk = 0; kk < kBlk / 16; ++kk) {
+                        if (kk == 0)
+                            mma_ts_w<false, -1>(tmem + kColDV, tmem + kColS, dm, kDescHi, kIdescTS, i > 0 ? 1u : 0u);
+                        else
+                            mma_ts_w<false, 1>(tmem + kColDV, tmem + kColS + 64 * (kk >> 2) + 8 * (kk & 3),
+                                               dm + 128 * kk, kDescHi, kIdescTS);
+                    }
                     // next block's scores: the P/dS warps keep P_i in registers
                     if constexpr (more) {
                         issue_s(s1);
@@ -422,9 +438,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                     tc_fence_after();
                     // dK += dS^T Q_i
 #pragma unroll
-                    for (int kk = 0; kk < kBlk / 16; ++kk)
-                        mma_bf16_ts(tmem + kColDK, tmem + kColDP + 64 * (kk >> 2) + 8 * (kk & 3),
-                                    sdesc_sw128(sQ + 2048 * kk, 16384, 1024), kIdescTS, (i > 0) || (kk > 0));
+                    for (int kk = 0; kk < kBlk / 16; ++kk) {
+                        if (kk == 0)
+                            mma_ts_w<false, -1>(tmem + kColDK, tmem + kColDP, qm, kDescHi, kIdescTS, i > 0 ? 1u : 0u);
+                        else
+                            mma_ts_w<false, 1>(tmem + kColDK, tmem + kColDP + 64 * (kk >> 2) + 8 * (kk & 3),
+                                               qm + 128 * kk, kDescHi, kIdescTS);
+                    }
                     // Q_i, dO_i, lse_i, delta_i consumed.  At d = 64 the item's last block hands
                     // its ring stage to the epilogue instead, which stages dV and dK in it and
                     // releases it once the TMA stores have read them.
@@ -462,7 +482,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             for (int k = 0, x = item_x(0); x < n_items && ok; x = item_x(++k), ++kc) {
                 const Item I = item_at(x);
                 const int kb = kc % C::kKBufs;
-                const uint32_t sK = sb + kOffK + kb * kTile;
+                constexpr uint32_t kDescHi = sdesc_sw128_hi(1024);
+                const uint32_t k_mn = sdesc_sw128_lo(sb + kOffK + kb * kTile, 16384);
                 ok = mbar_wait(smem_u32(&bars.k_full[kb]), (kc / C::kKBufs) & 1, lim, &abort_flag);
                 for (int i = 0; i < I.n_it && ok; ++i) {
                     const int gi = g + i, b = gi & 1;
@@ -471,11 +492,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                         ok = mbar_wait(smem_u32(&bars.dq_free[b]), ((gi >> 1) & 1) ^ 1, lim, &abort_flag);
                     if (!ok) break;
                     tc_fence_after();
-                    const uint32_t sDS = sb + kOffDS + b * kDSBytes;
+                    const uint32_t ds_mn = sdesc_sw128_lo(sb + kOffDS + b * kDSBytes, 16384);
 #pragma unroll
-                    for (int kk = 0; kk < kBlk / 16; ++kk)
-                        mma_bf16_ss(tmem + kColDQ + 64 * b, sdesc_sw128(sDS + 2048 * kk, 16384, 1024),
-                                    sdesc_sw128(sK + 2048 * kk, 16384, 1024), kIdescDQ, kk > 0);
+                    for (int kk = 0; kk < kBlk / 16; ++kk) {
+                        if (kk == 0)
+                            mma_ss_w<false, -1>(tmem + kColDQ + 64 * b, ds_mn, k_mn, kDescHi, kIdescDQ, 0u);
+                        else
+                            mma_ss_w<false, 1>(tmem + kColDQ + 64 * b, ds_mn + 128 * kk, k_mn + 128 * kk,
+                                               kDescHi, kIdescDQ);
+                    }
                     mma_commit(smem_u32(&bars.dq_full[b]));  // also: dS buffer b consumed
                 }
                 if (!ok) break;
