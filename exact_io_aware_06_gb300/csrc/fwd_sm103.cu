@@ -24,6 +24,11 @@
 //     alternate with the tensor core (ping-pong).  MMAs issued by one thread
 //     run in order, so the commit that publishes S_t(j+1) also proves that
 //     O_t += P_t(j) V_j is finished; the softmax warps may then rescale O_t.
+//   * E4M3: P_t goes to a 16 KB shared-memory tile instead (S and O of both tiles
+//     fill TMEM), and the P V MMA reads it from there.  S_t(j+1) is then issued as
+//     soon as the softmax warps have read S_t(j) out of TMEM (s_free), ahead of
+//     O_t += P_t(j) V_j; a pv_done commit after each P V MMA tells the softmax
+//     warps when P_t's tile may be rewritten and O_t rescaled.
 //   * Lazy rescale: the reference max used for exp2 moves only when a row's
 //     block max exceeds it by more than kTau (log2 units).  O and l always share
 //     the same reference, so the result is exact for any threshold; p stays
@@ -87,7 +92,13 @@ struct Cfg {
     static constexpr int kOffQ = 0;
     static constexpr int kOffK = 2 * kTileBytes;
     static constexpr int kOffV = kOffK + kStages * kTileBytes;
-    static constexpr int kSmemBytes = kOffV + kStages * kTileBytes;
+    // E4M3: P_t goes to shared memory (one 128 x 128-byte swizzled tile per query tile), so
+    // that S_t(j+1) can be computed into S_t's TMEM columns while the softmax warps still turn
+    // S_t(j) into P_t(j); S and O of both tiles already take all 512 TMEM columns.
+    static constexpr bool kPsmem = FP8;
+    static constexpr int kPBytes = kBM * kBN;              // E4M3 P tile
+    static constexpr int kOffP = kOffV + kStages * kTileBytes;
+    static constexpr int kSmemBytes = kOffP + (kPsmem ? 2 * kPBytes : 0);
     static constexpr int kSmemAlloc = kSmemBytes + 1024;   // slack for 1 KB alignment
     // TMEM columns
     static constexpr uint32_t kColS0 = 0, kColS1 = 128;
@@ -104,6 +115,7 @@ struct Bars {
     uint64_t k_full[kStages], k_empty[kStages];
     uint64_t v_full[kStages], v_empty[kStages];
     uint64_t s_full[2], p_full[2], o_done[2];
+    uint64_t s_free[2], pv_done[2];  // kPsmem: S_t read out of TMEM; O_t += P_t V done
     uint64_t o_staged[2];  // a tile's O rows are in shared memory (bf16 outputs)
     uint64_t drain;
 };
@@ -236,6 +248,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&bars.s_full[t]), 1);
             mbar_init(smem_u32(&bars.p_full[t]), 128);
             mbar_init(smem_u32(&bars.o_done[t]), 1);
+            mbar_init(smem_u32(&bars.s_free[t]), 128);
+            mbar_init(smem_u32(&bars.pv_done[t]), 1);
             mbar_init(smem_u32(&bars.o_staged[t]), 128);
         }
         mbar_init(smem_u32(&bars.drain), 1);
@@ -344,6 +358,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                                          kDescHi, C::kIdescO);
                 }
             };
+            // kPsmem: O_t += P_t V with P_t from its shared-memory tile (K-major, 128-byte rows)
+            const uint32_t p_lo0 = sdesc_sw128_lo(smem_base + C::kOffP, 16);
+            auto issue_pv_s = [&](uint32_t p_lo, int s, uint32_t colO, bool acc) {
+                const uint32_t vl = v_lo + s * (C::kTileBytes >> 4);
+#pragma unroll
+                for (int kk = 0; kk < kBN / C::kKStep; ++kk) {
+                    if (kk == 0)
+                        mma_ss_w<FP8, -1>(tmem + colO, p_lo, vl, kDescHi, C::kIdescO, acc ? 1u : 0u);
+                    else
+                        mma_ss_w<FP8, 1>(tmem + colO, p_lo + ((kk * C::kStepBytes) >> 4),
+                                         vl + ((kk * C::kKStep * 128) >> 4), kDescHi, C::kIdescO);
+                }
+            };
             if (SHARD && n_kv == 0) ok = false;  // nothing to multiply; not an error
             if (ok) ok = mbar_wait(smem_u32(&bars.k_full[0]), 0, lim, &abort_flag);
             if (ok) {
@@ -354,7 +381,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(smem_u32(&bars.s_full[1]));
                 mma_commit(smem_u32(&bars.k_empty[0]));
             }
-            for (int j = 0; j < n_kv && ok; ++j) {
+            // kPsmem: per block j, S_0(j+1) and S_1(j+1) as soon as the softmax warps have read
+            // S_t(j) out of TMEM, then O_t += P_t(j) V_j as each P_t(j) is published.
+            for (int j = 0; C::kPsmem && j < n_kv && ok; ++j) {
+                const int s = j % kStages;
+                const uint32_t ph = (j / kStages) & 1;
+                const int s1 = (j + 1) % kStages;
+                const uint32_t ph1 = ((j + 1) / kStages) & 1;
+                const bool more = (j + 1 < n_kv);
+                if (more) {
+                    ok = mbar_wait(smem_u32(&bars.k_full[s1]), ph1, lim, &abort_flag);
+                    if (ok) ok = mbar_wait(smem_u32(&bars.s_free[0]), j & 1, lim, &abort_flag);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_s(q_lo0, s1, C::kColS0);
+                    mma_commit(smem_u32(&bars.s_full[0]));
+                    ok = mbar_wait(smem_u32(&bars.s_free[1]), j & 1, lim, &abort_flag);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_s(q_lo1, s1, C::kColS1);
+                    mma_commit(smem_u32(&bars.s_full[1]));
+                    mma_commit(smem_u32(&bars.k_empty[s1]));
+                }
+                ok = mbar_wait(smem_u32(&bars.v_full[s]), ph, lim, &abort_flag);
+                if (ok) ok = mbar_wait(smem_u32(&bars.p_full[0]), j & 1, lim, &abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+                issue_pv_s(p_lo0, s, C::kColO0, j > 0);
+                mma_commit(smem_u32(more ? &bars.pv_done[0] : &bars.o_done[0]));
+                ok = mbar_wait(smem_u32(&bars.p_full[1]), j & 1, lim, &abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+                issue_pv_s(p_lo0 + (C::kPBytes >> 4), s, C::kColO1, j > 0);
+                mma_commit(smem_u32(&bars.v_empty[s]));
+                mma_commit(smem_u32(more ? &bars.pv_done[1] : &bars.o_done[1]));
+            }
+            for (int j = 0; !C::kPsmem && j < n_kv && ok; ++j) {
                 const int s = j % kStages;
                 const uint32_t ph = (j / kStages) & 1;
                 const int s1 = (j + 1) % kStages;
@@ -458,6 +520,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld32_at<64>(lane_base + colS + 64, r);
             tmem_ld32_at<96>(lane_base + colS + 96, r);
             tmem_wait_ld_fence(r);
+            if constexpr (C::kPsmem) {
+                // S_t(j) is in registers: its columns may take S_t(j+1)
+                tc_fence_before();
+                mbar_arrive(smem_u32(&bars.s_free[t]));
+            }
 
             const int kv0 = j * kBN;
             const int qlast = qrow + delta;  // last key this row reaches when causal
@@ -480,6 +547,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float ref = (m_ref == -INFINITY) ? 0.f : m_ref;
             const float2 c2 = make_float2(cj, cj), nref2 = make_float2(bj - ref, bj - ref);
+            if (C::kPsmem && j > 0) {
+                // P_t(j) replaces P_t(j-1), and O_t may be rescaled, once O_t += P_t(j-1) V
+                // has completed
+                ok = mbar_wait(smem_u32(&bars.pv_done[t]), (j - 1) & 1, lim, &abort_flag);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
+            }
             float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0;
             if (FP8) {
                 uint32_t pk[32];
@@ -495,7 +570,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     acc1 = __fadd2_rn(acc1, p23);
                     pk[i] = pack_e4m3x4(p01.x, p01.y, p23.x, p23.y);
                 }
-                tmem_st32(lane_base + colS, pk);
+                if constexpr (C::kPsmem) {
+                    // this row's 128 bytes in the 128-byte swizzle the MMA reads (16-byte
+                    // granule g of row r at g ^ (r % 8)), then visible to the tensor core
+                    const uint32_t prow = smem_base + C::kOffP + t * C::kPBytes + row_in_tile * 128;
+#pragma unroll
+                    for (int g = 0; g < 8; ++g)
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + ((g ^ (row_in_tile & 7)) * 16)),
+                                     "r"(pk[4 * g]), "r"(pk[4 * g + 1]), "r"(pk[4 * g + 2]), "r"(pk[4 * g + 3])
+                                     : "memory");
+                    fence_proxy_async_smem();
+                } else {
+                    tmem_st32(lane_base + colS, pk);
+                }
             } else {
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
@@ -517,7 +604,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (j > 0 && __any_sync(0xffffffffu, bump)) {
                 // O_t += P V of the previous block has completed (it precedes S_t(j) in
-                // issue order), so O_t can be rescaled in place before P_t(j) is published.
+                // issue order, or with P in shared memory pv_done said so above), so O_t
+                // can be rescaled in place before P_t(j) is published.
 #pragma unroll
                 for (int q4 = 0; q4 < D / 32; ++q4) {
                     uint32_t ov[32];
