@@ -22,11 +22,6 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
-__device__ __forceinline__ uint32_t elect_one_lane() {
-    // lane 0 of the (fully active) warp
-    return (threadIdx.x & 31u) == 0u;
-}
-
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -92,22 +87,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
     }
 }
 
-// mbar_wait for a thread whose waits are long and not on the critical path (a producer
-// that runs far ahead): between polls it sleeps for about `sleep_ns`, leaving the issue
-// slots of its sub-partition to the warps that compute.
-__device__ __forceinline__ bool mbar_wait_sleepy(uint32_t bar, uint32_t parity, uint64_t limit_ns,
-                                                 const volatile int* abort, uint32_t sleep_ns) {
-    if (mbar_test_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-#pragma unroll 1
-    while (true) {
-        if (mbar_test_wait(bar, parity)) return true;
-        if (*abort) return false;
-        if (globaltimer_ns() - t0 > limit_ns) return false;
-        __nanosleep(sleep_ns);
-    }
-}
-
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -158,21 +137,6 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// Shared-memory matrix descriptor, 128-byte swizzle (tiles 1024-byte aligned).
-//  bits  0-13 start address >> 4      bits 16-29 leading-dim byte offset >> 4
-//  bits 32-45 stride-dim byte off >> 4 bits 46-48 fixed 0b001
-//  bits 49-51 base offset (0)          bit  52    LBO mode (0)
-//  bits 61-63 swizzle (2 = 128B)
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-    uint64_t d = 0;
-    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
-    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
-    d |= static_cast<uint64_t>(1) << 46;
-    d |= static_cast<uint64_t>(2) << 61;
-    return d;
-}
-
 // Instruction descriptor for kind::f16 (D f32; A/B f16 or bf16) and
 // kind::f8f6f4 with E4M3 operands.
 //  bits 4-5 D format (1 = f32); 7-9 A format; 10-12 B format;
@@ -188,51 +152,17 @@ __host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N, bool a_mn, bool 
            (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// D[tmem] (+)= A[smem] * B[smem]
-__device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-// D[tmem] (+)= A[tmem] * B[smem]
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-__device__ __forceinline__ void mma_e4m3_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-__device__ __forceinline__ void mma_e4m3_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// sdesc_sw128 split into its two 32-bit words: the low word holds the start address and
-// the leading byte offset, the high word the stride byte offset and the fixed fields.  An
-// issue loop computes an operand's low word once and adds (byte offset / 16) per K step:
-// the 14-bit address field cannot overflow, shared addresses being below 2^18.  Issuing
-// MMAs back to back then costs the issuing thread one add per operand instead of a
-// 64-bit descriptor build.
+// Shared-memory matrix descriptor, 128-byte swizzle (tiles 1024-byte aligned):
+//  bits  0-13 start address >> 4      bits 16-29 leading-dim byte offset >> 4
+//  bits 32-45 stride-dim byte off >> 4 bits 46-48 fixed 0b001
+//  bits 49-51 base offset (0)          bit  52    LBO mode (0)
+//  bits 61-63 swizzle (2 = 128B)
+// kept as its two 32-bit words: the low word holds the start address and the leading byte
+// offset, the high word the stride byte offset and the fixed fields.  An issue loop
+// computes an operand's low word once and adds (byte offset / 16) per K step: the 14-bit
+// address field cannot overflow, shared addresses being below 2^18.  Issuing MMAs back to
+// back then costs the issuing thread one add per operand instead of a 64-bit descriptor
+// build.
 __device__ __forceinline__ uint32_t sdesc_sw128_lo(uint32_t saddr, uint32_t lbo) {
     return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
 }
@@ -350,16 +280,6 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[N]) {
     for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
 }
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
-        : FA_R8(0), FA_R8(8)
-        : "r"(taddr)
-        : "memory");
-}
-
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
@@ -374,13 +294,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
         "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
         FA_W8(0), FA_W8(8)
-        : "memory");
-}
-
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
-        FA_W8(0)
         : "memory");
 }
 
