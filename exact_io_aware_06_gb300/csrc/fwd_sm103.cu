@@ -13,7 +13,8 @@
 //
 // GB300 design (not the A100/H100 designs the pages sketch):
 //   * CTA = 2 query tiles of 128 rows (one head), 12 warps:
-//       warp 0      TMA producer: Q once, then K_j / V_j into 2-stage rings
+//       warp 0      TMA producer: Q once, then K and V into 2-stage rings (bf16: V_j
+//                   and K_{j+1} as one bundle on one barrier; E4M3: each on its own)
 //       warp 1      MMA issuer (one thread) + TMEM owner
 //       warps 4-7   softmax for query tile 0, warps 8-11 for query tile 1
 //   * TMEM (512 columns): S_t (128 fp32 columns per tile), O_t (d columns);
@@ -289,39 +290,71 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 qf, c * C::kBoxX, r0 + t * kBM, bh);
             int issued = 0;
             bool ok = true;
-            for (int j = 0; j < n_kv && ok; ++j) {
-                const int s = j % kStages;
-                const uint32_t ph = ((j / kStages) & 1) ^ 1;
-                if (j >= kStages && !mbar_wait(smem_u32(&bars.k_empty[s]), ph, lim, &abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t kf = smem_u32(&bars.k_full[s]);
-                mbar_arrive_expect_tx(kf, C::kTileBytes);
-                for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_3d(smem_base + C::kOffK + s * C::kTileBytes + c * C::kChunkBytes, &tm_k,
-                                kf, c * C::kBoxX, j * kBN, bh_kv);
-                if (j >= kStages && !mbar_wait(smem_u32(&bars.v_empty[s]), ph, lim, &abort_flag)) {
-                    issued = 2 * j + 1;
-                    ok = false;
-                    break;
-                }
-                const uint32_t vf = smem_u32(&bars.v_full[s]);
-                mbar_arrive_expect_tx(vf, C::kTileBytes);
-                for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_3d(smem_base + C::kOffV + s * C::kTileBytes + c * C::kChunkBytes, &tm_v,
-                                vf, c * C::kBoxX, j * kBN, bh_kv);
-                issued = 2 * j + 2;
-            }
-            if (!ok) record_timeout(args.ctl, &abort_flag);
-            // drain: Q and the newest load of every stage have landed before exit
             const volatile int never = 0;
-            mbar_wait(qf, 0, kDrainWaitNs, &never);
-            for (int x = max(0, issued - 2 * kStages); x < issued; ++x) {
-                const int j = x / 2;
-                const int s = j % kStages;
-                const uint32_t bar = (x & 1) ? smem_u32(&bars.v_full[s]) : smem_u32(&bars.k_full[s]);
-                mbar_wait(bar, (j / kStages) & 1, kDrainWaitNs, &never);
+            if constexpr (!C::kPsmem) {
+                // bf16: bundle n = {K_n (n < n_kv), V_{n-1} (n >= 1)} in slot n % kStages on
+                // one barrier.  The MMA thread issues P V_j right before S(j+1), so it needs
+                // V_j and K_{j+1} together, and both are last read by S_1(j+1).
+                for (int n = 0; n_kv > 0 && n <= n_kv; ++n) {
+                    const int u = n % kStages;
+                    if (n >= kStages &&
+                        !mbar_wait(smem_u32(&bars.k_empty[u]), ((n / kStages) & 1) ^ 1, lim, &abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(&bars.k_full[u]);
+                    mbar_arrive_expect_tx(fb, ((n < n_kv ? 1 : 0) + (n >= 1 ? 1 : 0)) * C::kTileBytes);
+                    if (n < n_kv)
+                        for (int c = 0; c < C::kChunks; ++c)
+                            tma_load_3d(smem_base + C::kOffK + u * C::kTileBytes + c * C::kChunkBytes, &tm_k,
+                                        fb, c * C::kBoxX, n * kBN, bh_kv);
+                    if (n >= 1)
+                        for (int c = 0; c < C::kChunks; ++c)
+                            tma_load_3d(smem_base + C::kOffV + u * C::kTileBytes + c * C::kChunkBytes, &tm_v,
+                                        fb, c * C::kBoxX, (n - 1) * kBN, bh_kv);
+                    issued = n + 1;
+                }
+                if (!ok) record_timeout(args.ctl, &abort_flag);
+                // drain: Q and the newest bundle of every slot have landed before exit
+                mbar_wait(qf, 0, kDrainWaitNs, &never);
+                for (int n = max(0, issued - kStages); n < issued; ++n)
+                    mbar_wait(smem_u32(&bars.k_full[n % kStages]), (n / kStages) & 1, kDrainWaitNs, &never);
+            } else {
+                // E4M3: K_j and V_j in their own rings (S_t(j+1) needs K_{j+1} well before
+                // P_t(j) V_j needs V_j)
+                for (int j = 0; j < n_kv && ok; ++j) {
+                    const int s = j % kStages;
+                    const uint32_t ph = ((j / kStages) & 1) ^ 1;
+                    if (j >= kStages && !mbar_wait(smem_u32(&bars.k_empty[s]), ph, lim, &abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t kf = smem_u32(&bars.k_full[s]);
+                    mbar_arrive_expect_tx(kf, C::kTileBytes);
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_load_3d(smem_base + C::kOffK + s * C::kTileBytes + c * C::kChunkBytes, &tm_k,
+                                    kf, c * C::kBoxX, j * kBN, bh_kv);
+                    if (j >= kStages && !mbar_wait(smem_u32(&bars.v_empty[s]), ph, lim, &abort_flag)) {
+                        issued = 2 * j + 1;
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t vf = smem_u32(&bars.v_full[s]);
+                    mbar_arrive_expect_tx(vf, C::kTileBytes);
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_load_3d(smem_base + C::kOffV + s * C::kTileBytes + c * C::kChunkBytes, &tm_v,
+                                    vf, c * C::kBoxX, j * kBN, bh_kv);
+                    issued = 2 * j + 2;
+                }
+                if (!ok) record_timeout(args.ctl, &abort_flag);
+                // drain: Q and the newest load of every stage have landed before exit
+                mbar_wait(qf, 0, kDrainWaitNs, &never);
+                for (int x = max(0, issued - 2 * kStages); x < issued; ++x) {
+                    const int j = x / 2;
+                    const int s = j % kStages;
+                    const uint32_t bar = (x & 1) ? smem_u32(&bars.v_full[s]) : smem_u32(&bars.k_full[s]);
+                    mbar_wait(bar, (j / kStages) & 1, kDrainWaitNs, &never);
+                }
             }
         }
     } else if (warp == 1) {
@@ -416,22 +449,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(smem_u32(&bars.v_empty[s]));
                 mma_commit(smem_u32(more ? &bars.pv_done[1] : &bars.o_done[1]));
             }
+            // bf16: per block j, one wait for bundle j+1 (V_j and K_{j+1}, slot u of both
+            // rings) and one release commit after its last reader, S_1(j+1).
             for (int j = 0; !C::kPsmem && j < n_kv && ok; ++j) {
-                const int s = j % kStages;
-                const uint32_t ph = (j / kStages) & 1;
-                const int s1 = (j + 1) % kStages;
-                const uint32_t ph1 = ((j + 1) / kStages) & 1;
+                const int u = (j + 1) % kStages;
+                const uint32_t phu = ((j + 1) / kStages) & 1;
                 const bool more = (j + 1 < n_kv);
-                ok = mbar_wait(smem_u32(&bars.v_full[s]), ph, lim, &abort_flag);
+                ok = mbar_wait(smem_u32(&bars.k_full[u]), phu, lim, &abort_flag);
                 if (ok) ok = mbar_wait(smem_u32(&bars.p_full[0]), j & 1, lim, &abort_flag);
                 if (!ok) break;
                 tc_fence_after();
-                issue_pv(C::kColS0, s, C::kColO0, j > 0);
+                issue_pv(C::kColS0, u, C::kColO0, j > 0);
                 if (more) {
-                    ok = mbar_wait(smem_u32(&bars.k_full[s1]), ph1, lim, &abort_flag);
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_s(q_lo0, s1, C::kColS0);
+                    issue_s(q_lo0, u, C::kColS0);
                     mma_commit(smem_u32(&bars.s_full[0]));
                 } else {
                     mma_commit(smem_u32(&bars.o_done[0]));
@@ -439,15 +469,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = mbar_wait(smem_u32(&bars.p_full[1]), j & 1, lim, &abort_flag);
                 if (!ok) break;
                 tc_fence_after();
-                issue_pv(C::kColS1, s, C::kColO1, j > 0);
-                mma_commit(smem_u32(&bars.v_empty[s]));
+                issue_pv(C::kColS1, u, C::kColO1, j > 0);
                 if (more) {
-                    issue_s(q_lo1, s1, C::kColS1);
+                    issue_s(q_lo1, u, C::kColS1);
                     mma_commit(smem_u32(&bars.s_full[1]));
-                    mma_commit(smem_u32(&bars.k_empty[s1]));
                 } else {
                     mma_commit(smem_u32(&bars.o_done[1]));
                 }
+                mma_commit(smem_u32(&bars.k_empty[u]));  // bundle j+1 read
             }
             if (!ok && (!SHARD || n_kv > 0)) record_timeout(args.ctl, &abort_flag);
             // drain every MMA this thread issued before TMEM is released
