@@ -13,8 +13,8 @@
 //
 // GB300 design (not the A100/H100 designs the pages sketch):
 //   * CTA = 2 query tiles of 128 rows (one head), 12 warps:
-//       warp 0      TMA producer: Q once, then K and V into 2-stage rings (bf16: V_j
-//                   and K_{j+1} as one bundle on one barrier; E4M3: each on its own)
+//       warp 0      TMA producer: Q once, then V_j and K_{j+1} as one bundle on one
+//                   barrier into 2-stage rings
 //       warp 1      MMA issuer (one thread) + TMEM owner
 //       warps 4-7   softmax for query tile 0, warps 8-11 for query tile 1
 //   * TMEM (512 columns): S_t (128 fp32 columns per tile), O_t (d columns);
@@ -113,8 +113,7 @@ struct Cfg {
 
 struct Bars {
     uint64_t q_full;
-    uint64_t k_full[kStages], k_empty[kStages];
-    uint64_t v_full[kStages], v_empty[kStages];
+    uint64_t kv_full[kStages], kv_empty[kStages];  // ring slot u: bundle n (n % kStages == u)
     uint64_t s_full[2], p_full[2], o_done[2];
     uint64_t s_free[2], pv_done[2];  // kPsmem: S_t read out of TMEM; O_t += P_t V done
     uint64_t o_staged[2];  // a tile's O rows are in shared memory (bf16 outputs)
@@ -240,10 +239,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         abort_flag = 0;
         mbar_init(smem_u32(&bars.q_full), 1);
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(smem_u32(&bars.k_full[s]), 1);
-            mbar_init(smem_u32(&bars.k_empty[s]), 1);
-            mbar_init(smem_u32(&bars.v_full[s]), 1);
-            mbar_init(smem_u32(&bars.v_empty[s]), 1);
+            mbar_init(smem_u32(&bars.kv_full[s]), 1);
+            mbar_init(smem_u32(&bars.kv_empty[s]), 1);
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(smem_u32(&bars.s_full[t]), 1);
@@ -291,71 +288,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             int issued = 0;
             bool ok = true;
             const volatile int never = 0;
-            if constexpr (!C::kPsmem) {
-                // bf16: bundle n = {K_n (n < n_kv), V_{n-1} (n >= 1)} in slot n % kStages on
-                // one barrier.  The MMA thread issues P V_j right before S(j+1), so it needs
-                // V_j and K_{j+1} together, and both are last read by S_1(j+1).
-                for (int n = 0; n_kv > 0 && n <= n_kv; ++n) {
-                    const int u = n % kStages;
-                    if (n >= kStages &&
-                        !mbar_wait(smem_u32(&bars.k_empty[u]), ((n / kStages) & 1) ^ 1, lim, &abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t fb = smem_u32(&bars.k_full[u]);
-                    mbar_arrive_expect_tx(fb, ((n < n_kv ? 1 : 0) + (n >= 1 ? 1 : 0)) * C::kTileBytes);
-                    if (n < n_kv)
-                        for (int c = 0; c < C::kChunks; ++c)
-                            tma_load_3d(smem_base + C::kOffK + u * C::kTileBytes + c * C::kChunkBytes, &tm_k,
-                                        fb, c * C::kBoxX, n * kBN, bh_kv);
-                    if (n >= 1)
-                        for (int c = 0; c < C::kChunks; ++c)
-                            tma_load_3d(smem_base + C::kOffV + u * C::kTileBytes + c * C::kChunkBytes, &tm_v,
-                                        fb, c * C::kBoxX, (n - 1) * kBN, bh_kv);
-                    issued = n + 1;
+            // Bundle n = {K_n (n < n_kv), V_{n-1} (n >= 1)} in slot n % kStages of both rings,
+            // on one barrier: the MMA thread waits once per block for V_j and K_{j+1}, and
+            // releases the slot once after their last reader.
+            for (int n = 0; n_kv > 0 && n <= n_kv; ++n) {
+                const int u = n % kStages;
+                if (n >= kStages &&
+                    !mbar_wait(smem_u32(&bars.kv_empty[u]), ((n / kStages) & 1) ^ 1, lim, &abort_flag)) {
+                    ok = false;
+                    break;
                 }
-                if (!ok) record_timeout(args.ctl, &abort_flag);
-                // drain: Q and the newest bundle of every slot have landed before exit
-                mbar_wait(qf, 0, kDrainWaitNs, &never);
-                for (int n = max(0, issued - kStages); n < issued; ++n)
-                    mbar_wait(smem_u32(&bars.k_full[n % kStages]), (n / kStages) & 1, kDrainWaitNs, &never);
-            } else {
-                // E4M3: K_j and V_j in their own rings (S_t(j+1) needs K_{j+1} well before
-                // P_t(j) V_j needs V_j)
-                for (int j = 0; j < n_kv && ok; ++j) {
-                    const int s = j % kStages;
-                    const uint32_t ph = ((j / kStages) & 1) ^ 1;
-                    if (j >= kStages && !mbar_wait(smem_u32(&bars.k_empty[s]), ph, lim, &abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t kf = smem_u32(&bars.k_full[s]);
-                    mbar_arrive_expect_tx(kf, C::kTileBytes);
+                const uint32_t fb = smem_u32(&bars.kv_full[u]);
+                mbar_arrive_expect_tx(fb, ((n < n_kv ? 1 : 0) + (n >= 1 ? 1 : 0)) * C::kTileBytes);
+                if (n < n_kv)
                     for (int c = 0; c < C::kChunks; ++c)
-                        tma_load_3d(smem_base + C::kOffK + s * C::kTileBytes + c * C::kChunkBytes, &tm_k,
-                                    kf, c * C::kBoxX, j * kBN, bh_kv);
-                    if (j >= kStages && !mbar_wait(smem_u32(&bars.v_empty[s]), ph, lim, &abort_flag)) {
-                        issued = 2 * j + 1;
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t vf = smem_u32(&bars.v_full[s]);
-                    mbar_arrive_expect_tx(vf, C::kTileBytes);
+                        tma_load_3d(smem_base + C::kOffK + u * C::kTileBytes + c * C::kChunkBytes, &tm_k,
+                                    fb, c * C::kBoxX, n * kBN, bh_kv);
+                if (n >= 1)
                     for (int c = 0; c < C::kChunks; ++c)
-                        tma_load_3d(smem_base + C::kOffV + s * C::kTileBytes + c * C::kChunkBytes, &tm_v,
-                                    vf, c * C::kBoxX, j * kBN, bh_kv);
-                    issued = 2 * j + 2;
-                }
-                if (!ok) record_timeout(args.ctl, &abort_flag);
-                // drain: Q and the newest load of every stage have landed before exit
-                mbar_wait(qf, 0, kDrainWaitNs, &never);
-                for (int x = max(0, issued - 2 * kStages); x < issued; ++x) {
-                    const int j = x / 2;
-                    const int s = j % kStages;
-                    const uint32_t bar = (x & 1) ? smem_u32(&bars.v_full[s]) : smem_u32(&bars.k_full[s]);
-                    mbar_wait(bar, (j / kStages) & 1, kDrainWaitNs, &never);
-                }
+                        tma_load_3d(smem_base + C::kOffV + u * C::kTileBytes + c * C::kChunkBytes, &tm_v,
+                                    fb, c * C::kBoxX, (n - 1) * kBN, bh_kv);
+                issued = n + 1;
             }
+            if (!ok) record_timeout(args.ctl, &abort_flag);
+            // drain: Q and the newest bundle of every slot have landed before exit
+            mbar_wait(qf, 0, kDrainWaitNs, &never);
+            for (int n = max(0, issued - kStages); n < issued; ++n)
+                mbar_wait(smem_u32(&bars.kv_full[n % kStages]), (n / kStages) & 1, kDrainWaitNs, &never);
         }
     } else if (warp == 1) {
         // ================================================================ MMA issuer
@@ -405,49 +364,47 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             };
             if (SHARD && n_kv == 0) ok = false;  // nothing to multiply; not an error
-            if (ok) ok = mbar_wait(smem_u32(&bars.k_full[0]), 0, lim, &abort_flag);
+            if (ok) ok = mbar_wait(smem_u32(&bars.kv_full[0]), 0, lim, &abort_flag);
             if (ok) {
                 tc_fence_after();
                 issue_s(q_lo0, 0, C::kColS0);
                 mma_commit(smem_u32(&bars.s_full[0]));
                 issue_s(q_lo1, 0, C::kColS1);
                 mma_commit(smem_u32(&bars.s_full[1]));
-                mma_commit(smem_u32(&bars.k_empty[0]));
+                mma_commit(smem_u32(&bars.kv_empty[0]));
             }
             // kPsmem: per block j, S_0(j+1) and S_1(j+1) as soon as the softmax warps have read
-            // S_t(j) out of TMEM, then O_t += P_t(j) V_j as each P_t(j) is published.
+            // S_t(j) out of TMEM, then O_t += P_t(j) V_j as each P_t(j) is published.  Bundle
+            // j+1 (K_{j+1}, V_j) is waited for once, and released after P_1(j) V_j.
             for (int j = 0; C::kPsmem && j < n_kv && ok; ++j) {
-                const int s = j % kStages;
-                const uint32_t ph = (j / kStages) & 1;
-                const int s1 = (j + 1) % kStages;
-                const uint32_t ph1 = ((j + 1) / kStages) & 1;
+                const int u = (j + 1) % kStages;
+                const uint32_t phu = ((j + 1) / kStages) & 1;
                 const bool more = (j + 1 < n_kv);
+                ok = mbar_wait(smem_u32(&bars.kv_full[u]), phu, lim, &abort_flag);
+                if (!ok) break;
                 if (more) {
-                    ok = mbar_wait(smem_u32(&bars.k_full[s1]), ph1, lim, &abort_flag);
-                    if (ok) ok = mbar_wait(smem_u32(&bars.s_free[0]), j & 1, lim, &abort_flag);
+                    ok = mbar_wait(smem_u32(&bars.s_free[0]), j & 1, lim, &abort_flag);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_s(q_lo0, s1, C::kColS0);
+                    issue_s(q_lo0, u, C::kColS0);
                     mma_commit(smem_u32(&bars.s_full[0]));
                     ok = mbar_wait(smem_u32(&bars.s_free[1]), j & 1, lim, &abort_flag);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_s(q_lo1, s1, C::kColS1);
+                    issue_s(q_lo1, u, C::kColS1);
                     mma_commit(smem_u32(&bars.s_full[1]));
-                    mma_commit(smem_u32(&bars.k_empty[s1]));
                 }
-                ok = mbar_wait(smem_u32(&bars.v_full[s]), ph, lim, &abort_flag);
-                if (ok) ok = mbar_wait(smem_u32(&bars.p_full[0]), j & 1, lim, &abort_flag);
+                ok = mbar_wait(smem_u32(&bars.p_full[0]), j & 1, lim, &abort_flag);
                 if (!ok) break;
                 tc_fence_after();
-                issue_pv_s(p_lo0, s, C::kColO0, j > 0);
+                issue_pv_s(p_lo0, u, C::kColO0, j > 0);
                 mma_commit(smem_u32(more ? &bars.pv_done[0] : &bars.o_done[0]));
                 ok = mbar_wait(smem_u32(&bars.p_full[1]), j & 1, lim, &abort_flag);
                 if (!ok) break;
                 tc_fence_after();
-                issue_pv_s(p_lo0 + (C::kPBytes >> 4), s, C::kColO1, j > 0);
-                mma_commit(smem_u32(&bars.v_empty[s]));
+                issue_pv_s(p_lo0 + (C::kPBytes >> 4), u, C::kColO1, j > 0);
                 mma_commit(smem_u32(more ? &bars.pv_done[1] : &bars.o_done[1]));
+                mma_commit(smem_u32(&bars.kv_empty[u]));  // bundle j+1 read
             }
             // bf16: per block j, one wait for bundle j+1 (V_j and K_{j+1}, slot u of both
             // rings) and one release commit after its last reader, S_1(j+1).
@@ -455,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int u = (j + 1) % kStages;
                 const uint32_t phu = ((j + 1) / kStages) & 1;
                 const bool more = (j + 1 < n_kv);
-                ok = mbar_wait(smem_u32(&bars.k_full[u]), phu, lim, &abort_flag);
+                ok = mbar_wait(smem_u32(&bars.kv_full[u]), phu, lim, &abort_flag);
                 if (ok) ok = mbar_wait(smem_u32(&bars.p_full[0]), j & 1, lim, &abort_flag);
                 if (!ok) break;
                 tc_fence_after();
@@ -476,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
                     mma_commit(smem_u32(&bars.o_done[1]));
                 }
-                mma_commit(smem_u32(&bars.k_empty[u]));  // bundle j+1 read
+                mma_commit(smem_u32(&bars.kv_empty[u]));  // bundle j+1 read
             }
             if (!ok && (!SHARD || n_kv > 0)) record_timeout(args.ctl, &abort_flag);
             // drain every MMA this thread issued before TMEM is released
