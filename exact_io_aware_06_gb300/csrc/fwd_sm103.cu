@@ -37,6 +37,7 @@
 //   * Every wait is bounded; on a timeout the kernel records it, drains its own
 //     TMA loads and MMAs, frees TMEM and exits.
 #include <cmath>
+#include <type_traits>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -373,68 +374,64 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(smem_u32(&bars.s_full[1]));
                 mma_commit(smem_u32(&bars.kv_empty[0]));
             }
-            // kPsmem: per block j, S_0(j+1) and S_1(j+1) as soon as the softmax warps have read
-            // S_t(j) out of TMEM, then O_t += P_t(j) V_j as each P_t(j) is published.  Bundle
-            // j+1 (K_{j+1}, V_j) is waited for once, and released after P_1(j) V_j.
-            for (int j = 0; C::kPsmem && j < n_kv && ok; ++j) {
+            // One K/V block j.  MORE (compile-time): a block j+1 follows, so S_t(j+1) is issued
+            // and P_t(j) V_j is followed by pv_done (E4M3); otherwise o_done.  The last block
+            // runs outside the loop, which keeps the loop body free of these branches.
+            //  - bf16: one wait for bundle j+1 (V_j and K_{j+1}, slot u of both rings), P_t V_j
+            //    then S_t(j+1) per tile, one release commit after S_1(j+1).
+            //  - E4M3 (kPsmem): S_0(j+1) and S_1(j+1) as soon as the softmax warps have read
+            //    S_t(j) out of TMEM, then O_t += P_t(j) V_j as each P_t(j) is published; the
+            //    bundle is released after P_1(j) V_j.
+            auto block = [&](int j, auto more_c) -> bool {
+                constexpr bool more = decltype(more_c)::value;
                 const int u = (j + 1) % kStages;
                 const uint32_t phu = ((j + 1) / kStages) & 1;
-                const bool more = (j + 1 < n_kv);
-                ok = mbar_wait(smem_u32(&bars.kv_full[u]), phu, lim, &abort_flag);
-                if (!ok) break;
-                if (more) {
-                    ok = mbar_wait(smem_u32(&bars.s_free[0]), j & 1, lim, &abort_flag);
-                    if (!ok) break;
+                if constexpr (C::kPsmem) {
+                    if (!mbar_wait(smem_u32(&bars.kv_full[u]), phu, lim, &abort_flag)) return false;
+                    if constexpr (more) {
+                        if (!mbar_wait(smem_u32(&bars.s_free[0]), j & 1, lim, &abort_flag)) return false;
+                        tc_fence_after();
+                        issue_s(q_lo0, u, C::kColS0);
+                        mma_commit(smem_u32(&bars.s_full[0]));
+                        if (!mbar_wait(smem_u32(&bars.s_free[1]), j & 1, lim, &abort_flag)) return false;
+                        tc_fence_after();
+                        issue_s(q_lo1, u, C::kColS1);
+                        mma_commit(smem_u32(&bars.s_full[1]));
+                    }
+                    if (!mbar_wait(smem_u32(&bars.p_full[0]), j & 1, lim, &abort_flag)) return false;
                     tc_fence_after();
-                    issue_s(q_lo0, u, C::kColS0);
-                    mma_commit(smem_u32(&bars.s_full[0]));
-                    ok = mbar_wait(smem_u32(&bars.s_free[1]), j & 1, lim, &abort_flag);
-                    if (!ok) break;
+                    issue_pv_s(p_lo0, u, C::kColO0, j > 0);
+                    mma_commit(smem_u32(more ? &bars.pv_done[0] : &bars.o_done[0]));
+                    if (!mbar_wait(smem_u32(&bars.p_full[1]), j & 1, lim, &abort_flag)) return false;
                     tc_fence_after();
-                    issue_s(q_lo1, u, C::kColS1);
-                    mma_commit(smem_u32(&bars.s_full[1]));
-                }
-                ok = mbar_wait(smem_u32(&bars.p_full[0]), j & 1, lim, &abort_flag);
-                if (!ok) break;
-                tc_fence_after();
-                issue_pv_s(p_lo0, u, C::kColO0, j > 0);
-                mma_commit(smem_u32(more ? &bars.pv_done[0] : &bars.o_done[0]));
-                ok = mbar_wait(smem_u32(&bars.p_full[1]), j & 1, lim, &abort_flag);
-                if (!ok) break;
-                tc_fence_after();
-                issue_pv_s(p_lo0 + (C::kPBytes >> 4), u, C::kColO1, j > 0);
-                mma_commit(smem_u32(more ? &bars.pv_done[1] : &bars.o_done[1]));
-                mma_commit(smem_u32(&bars.kv_empty[u]));  // bundle j+1 read
-            }
-            // bf16: per block j, one wait for bundle j+1 (V_j and K_{j+1}, slot u of both
-            // rings) and one release commit after its last reader, S_1(j+1).
-            for (int j = 0; !C::kPsmem && j < n_kv && ok; ++j) {
-                const int u = (j + 1) % kStages;
-                const uint32_t phu = ((j + 1) / kStages) & 1;
-                const bool more = (j + 1 < n_kv);
-                ok = mbar_wait(smem_u32(&bars.kv_full[u]), phu, lim, &abort_flag);
-                if (ok) ok = mbar_wait(smem_u32(&bars.p_full[0]), j & 1, lim, &abort_flag);
-                if (!ok) break;
-                tc_fence_after();
-                issue_pv(C::kColS0, u, C::kColO0, j > 0);
-                if (more) {
-                    issue_s(q_lo0, u, C::kColS0);
-                    mma_commit(smem_u32(&bars.s_full[0]));
+                    issue_pv_s(p_lo0 + (C::kPBytes >> 4), u, C::kColO1, j > 0);
+                    mma_commit(smem_u32(more ? &bars.pv_done[1] : &bars.o_done[1]));
                 } else {
-                    mma_commit(smem_u32(&bars.o_done[0]));
-                }
-                ok = mbar_wait(smem_u32(&bars.p_full[1]), j & 1, lim, &abort_flag);
-                if (!ok) break;
-                tc_fence_after();
-                issue_pv(C::kColS1, u, C::kColO1, j > 0);
-                if (more) {
-                    issue_s(q_lo1, u, C::kColS1);
-                    mma_commit(smem_u32(&bars.s_full[1]));
-                } else {
-                    mma_commit(smem_u32(&bars.o_done[1]));
+                    if (!mbar_wait(smem_u32(&bars.kv_full[u]), phu, lim, &abort_flag)) return false;
+                    if (!mbar_wait(smem_u32(&bars.p_full[0]), j & 1, lim, &abort_flag)) return false;
+                    tc_fence_after();
+                    issue_pv(C::kColS0, u, C::kColO0, j > 0);
+                    if constexpr (more) {
+                        issue_s(q_lo0, u, C::kColS0);
+                        mma_commit(smem_u32(&bars.s_full[0]));
+                    } else {
+                        mma_commit(smem_u32(&bars.o_done[0]));
+                    }
+                    if (!mbar_wait(smem_u32(&bars.p_full[1]), j & 1, lim, &abort_flag)) return false;
+                    tc_fence_after();
+                    issue_pv(C::kColS1, u, C::kColO1, j > 0);
+                    if constexpr (more) {
+                        issue_s(q_lo1, u, C::kColS1);
+                        mma_commit(smem_u32(&bars.s_full[1]));
+                    } else {
+                        mma_commit(smem_u32(&bars.o_done[1]));
+                    }
                 }
                 mma_commit(smem_u32(&bars.kv_empty[u]));  // bundle j+1 read
-            }
+                return true;
+            };
+            for (int j = 0; j + 1 < n_kv && ok; ++j) ok = block(j, std::true_type{});
+            if (ok && n_kv > 0) ok = block(n_kv - 1, std::false_type{});
             if (!ok && (!SHARD || n_kv > 0)) record_timeout(args.ctl, &abort_flag);
             // drain every MMA this thread issued before TMEM is released
             mma_commit(smem_u32(&bars.drain));
