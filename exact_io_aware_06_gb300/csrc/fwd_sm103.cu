@@ -12,7 +12,11 @@
 // the score step.
 //
 // GB300 design (not the A100/H100 designs the pages sketch):
-//   * CTA = 2 query tiles of 128 rows (one head), 12 warps:
+//   * Work item = 2 query tiles of 128 rows (one head).  bf16: one persistent CTA per SM
+//     works through items, its TMEM, barriers and K/V ring carrying over from item to
+//     item (the next item's Q and K/V load while one finishes); E4M3: one CTA per item.
+//     O is written by each softmax thread as its row; lse likewise.
+//   * 12 warps:
 //       warp 0      TMA producer: Q once, then V_j and K_{j+1} as one bundle on one
 //                   barrier into 2-stage rings
 //       warp 1      MMA issuer (one thread) + TMEM owner
@@ -48,18 +52,9 @@ namespace {
 
 constexpr int kBM = 128;         // query rows per tile
 constexpr int kBN = 128;         // keys per K/V block
-constexpr int kStages = 2;       // K ring and V ring depth
+constexpr int kStages = 2;       // K/V ring depth
 constexpr int kThreads = 384;    // 12 warps
 constexpr float kTau = 8.0f;     // lazy-rescale threshold, log2 units
-
-// Store a box from shared memory to global memory through the tensor map (TMA),
-// tracked by the thread's bulk async-group; rows past the tensor's end are not written.
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
-    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(src), "r"(x), "r"(y), "r"(z)
-                 : "memory");
-}
 
 struct FwdArgs {
     void* o;          // bf16 [BH][N][D], or float32 when o_f32
@@ -114,10 +109,10 @@ struct Cfg {
 
 struct Bars {
     uint64_t q_full;
-    uint64_t kv_full[kStages], kv_empty[kStages];  // ring slot u: bundle n (n % kStages == u)
+    uint64_t q_free;  // an item's last S MMAs have read the Q buffers
+    uint64_t kv_full[kStages], kv_empty[kStages];  // ring slot u: bundles n, n % kStages == u
     uint64_t s_full[2], p_full[2], o_done[2];
     uint64_t s_free[2], pv_done[2];  // kPsmem: S_t read out of TMEM; O_t += P_t V done
-    uint64_t o_staged[2];  // a tile's O rows are in shared memory (bf16 outputs)
     uint64_t drain;
 };
 
@@ -193,11 +188,19 @@ __device__ __forceinline__ float block_extreme(const uint32_t (&r)[128], bool wa
 // SHARD: forward over a key shard (N_kv keys, causal offset delta, float32 O,
 // rows that see no key); compiled separately so the plain forward carries none of it.
 // PB (FP8 only): the descales are per 128-row block of each head instead of per head.
+//
+// Persistent: a CTA works through (head, query-tile pair) items, its k-th item being
+// x = k * gridDim.x + (blockIdx.x, or gridDim.x - 1 - blockIdx.x in odd rounds).  Every
+// barrier counts its phases across items: per item with at least one key block (q_full,
+// q_free, o_done), per K/V block (s_full, p_full, s_free, pv_done) or per bundle
+// (kv_full, kv_empty), so TMEM, the barriers and the K/V ring carry over from one item to
+// the next, and the next item's Q and first bundle load while this item finishes.  An
+// item whose queries see no key (only in a causal key shard) involves neither the
+// producer nor the MMA thread: the softmax warps write its O = 0 and lse = -inf.
 template <int D, bool FP8, bool SHARD, bool PB = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                     const FwdArgs args) {
+                     const __grid_constant__ CUtensorMap tm_v, const FwdArgs args) {
     using C = Cfg<D, FP8>;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) Bars bars;
@@ -207,38 +210,58 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t smem_base =
         (smem_u32(smem_raw) + 1023u) & ~1023u;  // 1 KB aligned for the 128 B swizzle
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-
-    // ---- tile coordinates.  Non-causal: head-major, every pair of a head together (the
-    // head's K/V stays in L2).  Causal: a pair's work grows with its index, so CTAs are
-    // issued heaviest pair first across a group of hgrp heads (whose K/V fits in L2),
-    // group after group; head-major order would start the last heads' heaviest pairs
-    // near the end of the grid and leave a long tail.
-    int bh, pair;
-    if (args.causal) {
-        const int span = args.hgrp * args.n_pairs;
-        const int grp = blockIdx.x / span;
-        const int hg = min(args.hgrp, args.BH - grp * args.hgrp);  // heads in this group
-        const int xi = blockIdx.x - grp * span;
-        pair = args.n_pairs - 1 - xi / hg;
-        bh = grp * args.hgrp + xi % hg;
-    } else {
-        bh = blockIdx.x / args.n_pairs;
-        pair = args.n_pairs - 1 - (blockIdx.x % args.n_pairs);
-    }
-    // grouped-query attention: H / H_kv query heads share one K/V head
-    const int bh_kv = (bh / args.H) * args.H_kv + (bh % args.H) / (args.H / args.H_kv);
-    const int r0 = pair * 2 * kBM;
     const int N = args.N;
     const int N_kv = SHARD ? args.N_kv : N;
     const int delta = SHARD ? args.delta : 0;
-    // keys this pair of tiles can see; none at all when a causal key shard lies
-    // wholly after these queries
-    const int kv_end = args.causal ? min(N_kv, r0 + 2 * kBM + delta) : N_kv;
-    const int n_kv = (!SHARD || kv_end > 0) ? (kv_end + kBN - 1) / kBN : 0;
+    const int n_items = args.n_pairs * args.BH;
+    const int G = static_cast<int>(gridDim.x);
+    // E4M3 runs one CTA per item (see the launch); with a compile-time single pass every
+    // running counter below is a constant there
+    constexpr bool kPersist = !FP8;
+    constexpr int kItemsMax = kPersist ? 0x7fffffff : 1;
+
+    // this CTA's k-th item, dealt in alternating (snake) order so that no CTA always
+    // takes the heaviest item of a round (causal items are ordered heaviest first)
+    auto item_x = [&](int k) {
+        return k * G + ((k & 1) ? G - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x));
+    };
+    struct Item {
+        int bh, bh_kv, r0, n_kv;
+    };
+    // Item x's tile pair.  Non-causal: head-major, every pair of a head together (the
+    // head's K/V stays in L2).  Causal: a pair's work grows with its index, so items run
+    // heaviest pair first across a group of hgrp heads (whose K/V fits in L2), group
+    // after group; head-major order would leave the last heads' heaviest pairs for the
+    // end and a long tail.
+    auto item_at = [&](int x) {
+        int bh, pair;
+        if (args.causal) {
+            const int span = args.hgrp * args.n_pairs;
+            const int grp = x / span;
+            const int hg = min(args.hgrp, args.BH - grp * args.hgrp);  // heads in this group
+            const int xi = x - grp * span;
+            pair = args.n_pairs - 1 - xi / hg;
+            bh = grp * args.hgrp + xi % hg;
+        } else {
+            bh = x / args.n_pairs;
+            pair = args.n_pairs - 1 - (x % args.n_pairs);
+        }
+        Item I;
+        I.bh = bh;
+        // grouped-query attention: H / H_kv query heads share one K/V head
+        I.bh_kv = (bh / args.H) * args.H_kv + (bh % args.H) / (args.H / args.H_kv);
+        I.r0 = pair * 2 * kBM;
+        // keys this pair of tiles can see; none at all when a causal key shard lies
+        // wholly after these queries
+        const int kv_end = args.causal ? min(N_kv, I.r0 + 2 * kBM + delta) : N_kv;
+        I.n_kv = (!SHARD || kv_end > 0) ? (kv_end + kBN - 1) / kBN : 0;
+        return I;
+    };
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
         mbar_init(smem_u32(&bars.q_full), 1);
+        mbar_init(smem_u32(&bars.q_free), 1);
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&bars.kv_full[s]), 1);
             mbar_init(smem_u32(&bars.kv_empty[s]), 1);
@@ -249,7 +272,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&bars.o_done[t]), 1);
             mbar_init(smem_u32(&bars.s_free[t]), 128);
             mbar_init(smem_u32(&bars.pv_done[t]), 1);
-            mbar_init(smem_u32(&bars.o_staged[t]), 128);
         }
         mbar_init(smem_u32(&bars.drain), 1);
         fence_barrier_init();
@@ -281,47 +303,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ================================================================ TMA producer
         if (lane == 0) {
             const uint32_t qf = smem_u32(&bars.q_full);
-            mbar_arrive_expect_tx(qf, 2 * C::kTileBytes);
-            for (int t = 0; t < 2; ++t)
-                for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_3d(smem_base + C::kOffQ + t * C::kTileBytes + c * C::kChunkBytes, &tm_q,
-                                qf, c * C::kBoxX, r0 + t * kBM, bh);
-            int issued = 0;
+            int gb = 0;  // bundles issued, over all items
+            int kq = 0;  // items whose Q was issued (items with at least one key block)
             bool ok = true;
             const volatile int never = 0;
-            // Bundle n = {K_n (n < n_kv), V_{n-1} (n >= 1)} in slot n % kStages of both rings,
-            // on one barrier: the MMA thread waits once per block for V_j and K_{j+1}, and
-            // releases the slot once after their last reader.
-            for (int n = 0; n_kv > 0 && n <= n_kv; ++n) {
-                const int u = n % kStages;
-                if (n >= kStages &&
-                    !mbar_wait(smem_u32(&bars.kv_empty[u]), ((n / kStages) & 1) ^ 1, lim, &abort_flag)) {
+            for (int k = 0; ok && k < kItemsMax; ++k) {
+                const int x = item_x(k);
+                if (x >= n_items) break;
+                const Item I = item_at(x);
+                if (SHARD && I.n_kv == 0) continue;
+                // Q of this item once the last S MMAs of the previous one have read the Q buffers
+                if (kq > 0 && !mbar_wait(smem_u32(&bars.q_free), (kq - 1) & 1, lim, &abort_flag)) {
                     ok = false;
                     break;
                 }
-                const uint32_t fb = smem_u32(&bars.kv_full[u]);
-                mbar_arrive_expect_tx(fb, ((n < n_kv ? 1 : 0) + (n >= 1 ? 1 : 0)) * C::kTileBytes);
-                if (n < n_kv)
+                mbar_arrive_expect_tx(qf, 2 * C::kTileBytes);
+                for (int t = 0; t < 2; ++t)
                     for (int c = 0; c < C::kChunks; ++c)
-                        tma_load_3d(smem_base + C::kOffK + u * C::kTileBytes + c * C::kChunkBytes, &tm_k,
-                                    fb, c * C::kBoxX, n * kBN, bh_kv);
-                if (n >= 1)
-                    for (int c = 0; c < C::kChunks; ++c)
-                        tma_load_3d(smem_base + C::kOffV + u * C::kTileBytes + c * C::kChunkBytes, &tm_v,
-                                    fb, c * C::kBoxX, (n - 1) * kBN, bh_kv);
-                issued = n + 1;
+                        tma_load_3d(smem_base + C::kOffQ + t * C::kTileBytes + c * C::kChunkBytes, &tm_q,
+                                    qf, c * C::kBoxX, I.r0 + t * kBM, I.bh);
+                ++kq;
+                // Bundle n = {K_n (n < n_kv), V_{n-1} (n >= 1)} in slot gb % kStages of both
+                // rings, on one barrier: the MMA thread waits once per block for V_j and
+                // K_{j+1}, and releases the slot once after their last reader.
+                for (int n = 0; I.n_kv > 0 && n <= I.n_kv; ++n, ++gb) {
+                    const int u = gb % kStages;
+                    if (gb >= kStages &&
+                        !mbar_wait(smem_u32(&bars.kv_empty[u]), ((gb / kStages) & 1) ^ 1, lim, &abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(&bars.kv_full[u]);
+                    mbar_arrive_expect_tx(fb, ((n < I.n_kv ? 1 : 0) + (n >= 1 ? 1 : 0)) * C::kTileBytes);
+                    if (n < I.n_kv)
+                        for (int c = 0; c < C::kChunks; ++c)
+                            tma_load_3d(smem_base + C::kOffK + u * C::kTileBytes + c * C::kChunkBytes, &tm_k,
+                                        fb, c * C::kBoxX, n * kBN, I.bh_kv);
+                    if (n >= 1)
+                        for (int c = 0; c < C::kChunks; ++c)
+                            tma_load_3d(smem_base + C::kOffV + u * C::kTileBytes + c * C::kChunkBytes, &tm_v,
+                                        fb, c * C::kBoxX, (n - 1) * kBN, I.bh_kv);
+                }
             }
             if (!ok) record_timeout(args.ctl, &abort_flag);
-            // drain: Q and the newest bundle of every slot have landed before exit
-            mbar_wait(qf, 0, kDrainWaitNs, &never);
-            for (int n = max(0, issued - kStages); n < issued; ++n)
+            // drain: the last Q and the newest bundle of every slot have landed before exit
+            if (kq > 0) mbar_wait(qf, (kq - 1) & 1, kDrainWaitNs, &never);
+            for (int n = max(0, gb - kStages); n < gb; ++n)
                 mbar_wait(smem_u32(&bars.kv_full[n % kStages]), (n / kStages) & 1, kDrainWaitNs, &never);
         }
     } else if (warp == 1) {
         // ================================================================ MMA issuer
         if (lane == 0) {
             const uint32_t sQ0 = smem_base + C::kOffQ, sQ1 = sQ0 + C::kTileBytes;
-            bool ok = mbar_wait(smem_u32(&bars.q_full), 0, lim, &abort_flag);
             // Operand descriptors: the low words of Q_t and of stage 0 of the K and V rings
             // are computed once; each MMA adds its K step's offset (see sdesc_sw128_lo).
             constexpr uint32_t kDescHi = sdesc_sw128_hi(1024);
@@ -364,51 +397,50 @@ __global__ void __launch_bounds__(kThreads, 1)
                                          vl + ((kk * C::kKStep * 128) >> 4), kDescHi, C::kIdescO);
                 }
             };
-            if (SHARD && n_kv == 0) ok = false;  // nothing to multiply; not an error
-            if (ok) ok = mbar_wait(smem_u32(&bars.kv_full[0]), 0, lim, &abort_flag);
-            if (ok) {
-                tc_fence_after();
-                issue_s(q_lo0, 0, C::kColS0);
-                mma_commit(smem_u32(&bars.s_full[0]));
-                issue_s(q_lo1, 0, C::kColS1);
-                mma_commit(smem_u32(&bars.s_full[1]));
-                mma_commit(smem_u32(&bars.kv_empty[0]));
-            }
-            // One K/V block j.  MORE (compile-time): a block j+1 follows, so S_t(j+1) is issued
-            // and P_t(j) V_j is followed by pv_done (E4M3); otherwise o_done.  The last block
-            // runs outside the loop, which keeps the loop body free of these branches.
+            int gb = 0;  // bundle index of the current item's bundle 0, over all items
+            int gj = 0;  // index of the current item's first K/V block, over all items
+            bool ok = true;
+            // One K/V block j of the current item.  MORE (compile-time): a block j+1 follows,
+            // so S_t(j+1) is issued; otherwise o_done is committed.  LAST2: block j+1 is the
+            // item's last, so S_1(j+1) is the item's last read of Q (q_free).  The item's last
+            // two blocks run outside the loop, which keeps its body free of these branches.
             //  - bf16: one wait for bundle j+1 (V_j and K_{j+1}, slot u of both rings), P_t V_j
             //    then S_t(j+1) per tile, one release commit after S_1(j+1).
             //  - E4M3 (kPsmem): S_0(j+1) and S_1(j+1) as soon as the softmax warps have read
             //    S_t(j) out of TMEM, then O_t += P_t(j) V_j as each P_t(j) is published; the
             //    bundle is released after P_1(j) V_j.
-            auto block = [&](int j, auto more_c) -> bool {
-                constexpr bool more = decltype(more_c)::value;
-                const int u = (j + 1) % kStages;
-                const uint32_t phu = ((j + 1) / kStages) & 1;
+            // g1: index of bundle j+1 over all items; pj: parity of block j's per-block barriers
+            // (both passed by value, so the running counters stay out of the loop body)
+            auto block = [&](int j, int g1, uint32_t pj, auto more_c, auto last2_c) -> bool {
+                constexpr bool more = decltype(more_c)::value, last2 = decltype(last2_c)::value;
+                const int u = g1 % kStages;
+                const uint32_t phu = (g1 / kStages) & 1;
                 if constexpr (C::kPsmem) {
                     if (!mbar_wait(smem_u32(&bars.kv_full[u]), phu, lim, &abort_flag)) return false;
                     if constexpr (more) {
-                        if (!mbar_wait(smem_u32(&bars.s_free[0]), j & 1, lim, &abort_flag)) return false;
+                        if (!mbar_wait(smem_u32(&bars.s_free[0]), pj, lim, &abort_flag)) return false;
                         tc_fence_after();
                         issue_s(q_lo0, u, C::kColS0);
                         mma_commit(smem_u32(&bars.s_full[0]));
-                        if (!mbar_wait(smem_u32(&bars.s_free[1]), j & 1, lim, &abort_flag)) return false;
+                        if (!mbar_wait(smem_u32(&bars.s_free[1]), pj, lim, &abort_flag)) return false;
                         tc_fence_after();
                         issue_s(q_lo1, u, C::kColS1);
                         mma_commit(smem_u32(&bars.s_full[1]));
+                        if constexpr (last2) mma_commit(smem_u32(&bars.q_free));
                     }
-                    if (!mbar_wait(smem_u32(&bars.p_full[0]), j & 1, lim, &abort_flag)) return false;
+                    if (!mbar_wait(smem_u32(&bars.p_full[0]), pj, lim, &abort_flag)) return false;
                     tc_fence_after();
                     issue_pv_s(p_lo0, u, C::kColO0, j > 0);
-                    mma_commit(smem_u32(more ? &bars.pv_done[0] : &bars.o_done[0]));
-                    if (!mbar_wait(smem_u32(&bars.p_full[1]), j & 1, lim, &abort_flag)) return false;
+                    mma_commit(smem_u32(&bars.pv_done[0]));
+                    if constexpr (!more) mma_commit(smem_u32(&bars.o_done[0]));
+                    if (!mbar_wait(smem_u32(&bars.p_full[1]), pj, lim, &abort_flag)) return false;
                     tc_fence_after();
                     issue_pv_s(p_lo0 + (C::kPBytes >> 4), u, C::kColO1, j > 0);
-                    mma_commit(smem_u32(more ? &bars.pv_done[1] : &bars.o_done[1]));
+                    mma_commit(smem_u32(&bars.pv_done[1]));
+                    if constexpr (!more) mma_commit(smem_u32(&bars.o_done[1]));
                 } else {
                     if (!mbar_wait(smem_u32(&bars.kv_full[u]), phu, lim, &abort_flag)) return false;
-                    if (!mbar_wait(smem_u32(&bars.p_full[0]), j & 1, lim, &abort_flag)) return false;
+                    if (!mbar_wait(smem_u32(&bars.p_full[0]), pj, lim, &abort_flag)) return false;
                     tc_fence_after();
                     issue_pv(C::kColS0, u, C::kColO0, j > 0);
                     if constexpr (more) {
@@ -417,12 +449,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     } else {
                         mma_commit(smem_u32(&bars.o_done[0]));
                     }
-                    if (!mbar_wait(smem_u32(&bars.p_full[1]), j & 1, lim, &abort_flag)) return false;
+                    if (!mbar_wait(smem_u32(&bars.p_full[1]), pj, lim, &abort_flag)) return false;
                     tc_fence_after();
                     issue_pv(C::kColS1, u, C::kColO1, j > 0);
                     if constexpr (more) {
                         issue_s(q_lo1, u, C::kColS1);
                         mma_commit(smem_u32(&bars.s_full[1]));
+                        if constexpr (last2) mma_commit(smem_u32(&bars.q_free));
                     } else {
                         mma_commit(smem_u32(&bars.o_done[1]));
                     }
@@ -430,9 +463,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(smem_u32(&bars.kv_empty[u]));  // bundle j+1 read
                 return true;
             };
-            for (int j = 0; j + 1 < n_kv && ok; ++j) ok = block(j, std::true_type{});
-            if (ok && n_kv > 0) ok = block(n_kv - 1, std::false_type{});
-            if (!ok && (!SHARD || n_kv > 0)) record_timeout(args.ctl, &abort_flag);
+            using T = std::true_type;
+            using F = std::false_type;
+            int kq = 0;  // items with at least one key block done
+            for (int k = 0; ok && k < kItemsMax; ++k) {
+                const int x = item_x(k);
+                if (x >= n_items) break;
+                const Item I = item_at(x);
+                if (SHARD && I.n_kv == 0) continue;  // no key reaches these queries
+                ok = mbar_wait(smem_u32(&bars.q_full), kq & 1, lim, &abort_flag);
+                if (!ok) break;
+                // the item's first scores: bundle 0 holds K_0; with P in shared memory the
+                // previous item's last S_t must have been read out of TMEM first
+                ok = mbar_wait(smem_u32(&bars.kv_full[gb % kStages]), (gb / kStages) & 1, lim, &abort_flag);
+                if (ok && C::kPsmem && gj > 0) {
+                    ok = mbar_wait(smem_u32(&bars.s_free[0]), (gj - 1) & 1, lim, &abort_flag);
+                    if (ok) ok = mbar_wait(smem_u32(&bars.s_free[1]), (gj - 1) & 1, lim, &abort_flag);
+                }
+                if (!ok) break;
+                tc_fence_after();
+                issue_s(q_lo0, gb % kStages, C::kColS0);
+                mma_commit(smem_u32(&bars.s_full[0]));
+                issue_s(q_lo1, gb % kStages, C::kColS1);
+                mma_commit(smem_u32(&bars.s_full[1]));
+                if (I.n_kv == 1) mma_commit(smem_u32(&bars.q_free));
+                mma_commit(smem_u32(&bars.kv_empty[gb % kStages]));  // bundle 0 read
+                const int g0 = gb, j0 = gj;
+                int j = 0;
+                for (; j + 2 < I.n_kv && ok; ++j) ok = block(j, g0 + j + 1, (j0 + j) & 1, T{}, F{});
+                if (ok && I.n_kv >= 2) ok = block(I.n_kv - 2, g0 + I.n_kv - 1, (j0 + I.n_kv - 2) & 1, T{}, T{});
+                if (ok) ok = block(I.n_kv - 1, g0 + I.n_kv, (j0 + I.n_kv - 1) & 1, F{}, F{});
+                gb += I.n_kv + 1;
+                gj += I.n_kv;
+                ++kq;
+            }
+            if (!ok) record_timeout(args.ctl, &abort_flag);
             // drain every MMA this thread issued before TMEM is released
             mma_commit(smem_u32(&bars.drain));
             const volatile int never = 0;
@@ -446,245 +511,215 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = (warp - 4) / 4;              // query tile 0 or 1
         const int wq = warp % 4;                   // TMEM lane quarter
         const int row_in_tile = wq * 32 + lane;
-        const int qrow = r0 + t * kBM + row_in_tile;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
         const uint32_t colS = t ? C::kColS1 : C::kColS0;
         const uint32_t colO = t ? C::kColO1 : C::kColO0;
-        // per-head FP8 descales fold into the score constant and the output scale
-        float c = args.c_log2, o_scale = args.o_scale;
-        // per-block FP8 descales: this tile's Q factor folds into c, key block j's K factor
-        // into c_j = c * kd_j.  V's factor vd_j cannot be applied after P V has been
-        // accumulated, so it goes into P before the E4M3 rounding: P'_j = P_j vd_j / vd_max
-        // (at most P_j), by adding log2(vd_j / vd_max) <= 0 to the exponent; the row sum
-        // adds the block's sum times vd_max / vd_j, and O is scaled by vd_max at the end.
-        // The ratio is held at >= 2^-100, where P' is still exact in fp32, so that a zero
-        // factor keeps its block's mass in l.
-        const float* kd_blk = nullptr;
-        const float* vd_blk = nullptr;
-        float lg_vmax = 0.f;
-        if (PB) {
-            const int n_kb = (N_kv + kBN - 1) / kBN;
-            c *= args.qk_descale_q[static_cast<size_t>(bh) * ((N + kBM - 1) / kBM) + (r0 / kBM + t)];
-            kd_blk = args.qk_descale_k + static_cast<size_t>(bh_kv) * n_kb;
-            vd_blk = args.v_descale + static_cast<size_t>(bh_kv) * n_kb;
-            float vm = 0.f;
-            for (int x = lane; x < n_kb; x += 32) vm = fmaxf(vm, vd_blk[x]);
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, off));
-            o_scale = vm;
-            lg_vmax = lg2_approx(vm);
-        } else if (args.qk_descale_q) {
-            c *= args.qk_descale_q[bh] * args.qk_descale_k[bh_kv];
-            o_scale = args.v_descale[bh_kv];
-        }
-        const bool c_pos = c >= 0.f;
-        // a masked score must become -inf after the multiply by c
-        const uint32_t mask_bits = c_pos ? 0xff800000u : 0x7f800000u;
-        float m_ref = -INFINITY;  // reference max in log2 units
-        float l = 0.f;
+        int gj = 0;  // index of the current item's first K/V block, over all items
+        int kd = 0;  // items with at least one key block done
         bool ok = true;
-
-        for (int j = 0; j < n_kv; ++j) {
-            // key block j's factors (per-block FP8), loaded before the wait
-            float cj = c, bj = 0.f, inv_rj = 1.f;
+        for (int k = 0; ok && k < kItemsMax; ++k) {
+            const int x = item_x(k);
+            if (x >= n_items) break;
+            const Item I = item_at(x);
+            const int n_kv = I.n_kv;
+            const int qrow = I.r0 + t * kBM + row_in_tile;
+            // per-head FP8 descales fold into the score constant and the output scale
+            float c = args.c_log2, o_scale = args.o_scale;
+            // per-block FP8 descales: this tile's Q factor folds into c, key block j's K factor
+            // into c_j = c * kd_j.  V's factor vd_j cannot be applied after P V has been
+            // accumulated, so it goes into P before the E4M3 rounding: P'_j = P_j vd_j / vd_max
+            // (at most P_j), by adding log2(vd_j / vd_max) <= 0 to the exponent; the row sum
+            // adds the block's sum times vd_max / vd_j, and O is scaled by vd_max at the end.
+            // The ratio is held at >= 2^-100, where P' is still exact in fp32, so that a zero
+            // factor keeps its block's mass in l.
+            const float* kd_blk = nullptr;
+            const float* vd_blk = nullptr;
+            float lg_vmax = 0.f;
             if (PB) {
-                const float kdj = __ldg(kd_blk + j), vdj = __ldg(vd_blk + j);
-                cj = c * kdj;
-                bj = fmaxf(lg2_approx(vdj) - lg_vmax, -100.f);
-                inv_rj = ex2_approx(-bj);
+                const int n_kb = (N_kv + kBN - 1) / kBN;
+                c *= args.qk_descale_q[static_cast<size_t>(I.bh) * ((N + kBM - 1) / kBM) + (I.r0 / kBM + t)];
+                kd_blk = args.qk_descale_k + static_cast<size_t>(I.bh_kv) * n_kb;
+                vd_blk = args.v_descale + static_cast<size_t>(I.bh_kv) * n_kb;
+                float vm = 0.f;
+                for (int x = lane; x < n_kb; x += 32) vm = fmaxf(vm, vd_blk[x]);
+    #pragma unroll
+                for (int off = 16; off > 0; off >>= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, off));
+                o_scale = vm;
+                lg_vmax = lg2_approx(vm);
+            } else if (args.qk_descale_q) {
+                c *= args.qk_descale_q[I.bh] * args.qk_descale_k[I.bh_kv];
+                o_scale = args.v_descale[I.bh_kv];
             }
-            ok = mbar_wait(smem_u32(&bars.s_full[t]), j & 1, lim, &abort_flag);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            tc_fence_after();
-            uint32_t r[128];
-            tmem_ld32_at<0>(lane_base + colS, r);
-            tmem_ld32_at<32>(lane_base + colS + 32, r);
-            tmem_ld32_at<64>(lane_base + colS + 64, r);
-            tmem_ld32_at<96>(lane_base + colS + 96, r);
-            tmem_wait_ld_fence(r);
-            if constexpr (C::kPsmem) {
-                // S_t(j) is in registers: its columns may take S_t(j+1)
-                tc_fence_before();
-                mbar_arrive(smem_u32(&bars.s_free[t]));
-            }
+            const bool c_pos = c >= 0.f;
+            // a masked score must become -inf after the multiply by c
+            const uint32_t mask_bits = c_pos ? 0xff800000u : 0x7f800000u;
+            float m_ref = -INFINITY;  // reference max in log2 units
+            float l = 0.f;
 
-            const int kv0 = j * kBN;
-            const int qlast = qrow + delta;  // last key this row reaches when causal
-            if ((kv0 + kBN > N_kv) || (args.causal && kv0 + kBN - 1 > qlast)) {
-                // keys >= N_kv, and keys after this query row when causal, drop out
-                const int valid = min(N_kv - kv0, args.causal ? qlast - kv0 + 1 : kBN);
-#pragma unroll
-                for (int i = 0; i < 128; ++i)
-                    if (i >= valid) r[i] = mask_bits;
-            }
-            // block max of the scaled scores = c * (max of the raw scores) for c >= 0
-            const float mt = cj * block_extreme(r, c_pos);
-            // lazy rescale: move the reference only when the block max exceeds it by > kTau
-            float alpha = 1.f;
-            const bool bump = mt > m_ref + kTau;
-            if (bump) {
-                alpha = (m_ref == -INFINITY) ? 0.f : ex2_approx(m_ref - mt);
-                m_ref = mt;
-                l *= alpha;
-            }
-            const float ref = (m_ref == -INFINITY) ? 0.f : m_ref;
-            const float2 c2 = make_float2(cj, cj), nref2 = make_float2(bj - ref, bj - ref);
-            if (C::kPsmem && j > 0) {
-                // P_t(j) replaces P_t(j-1), and O_t may be rescaled, once O_t += P_t(j-1) V
-                // has completed
-                ok = mbar_wait(smem_u32(&bars.pv_done[t]), (j - 1) & 1, lim, &abort_flag);
+            for (int j = 0; j < n_kv; ++j) {
+                // key block j's factors (per-block FP8), loaded before the wait
+                float cj = c, bj = 0.f, inv_rj = 1.f;
+                if (PB) {
+                    const float kdj = __ldg(kd_blk + j), vdj = __ldg(vd_blk + j);
+                    cj = c * kdj;
+                    bj = fmaxf(lg2_approx(vdj) - lg_vmax, -100.f);
+                    inv_rj = ex2_approx(-bj);
+                }
+                ok = mbar_wait(smem_u32(&bars.s_full[t]), (gj + j) & 1, lim, &abort_flag);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();
-            }
-            float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0;
-            if (FP8) {
-                uint32_t pk[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float2 x01 = __ffma2_rn(
-                        make_float2(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1])), c2, nref2);
-                    const float2 x23 = __ffma2_rn(
-                        make_float2(__uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])), c2, nref2);
-                    const float2 p01 = make_float2(ex2_approx(x01.x), ex2_approx(x01.y));
-                    const float2 p23 = make_float2(ex2_approx(x23.x), ex2_approx(x23.y));
-                    acc0 = __fadd2_rn(acc0, p01);
-                    acc1 = __fadd2_rn(acc1, p23);
-                    pk[i] = pack_e4m3x4(p01.x, p01.y, p23.x, p23.y);
-                }
+                uint32_t r[128];
+                tmem_ld32_at<0>(lane_base + colS, r);
+                tmem_ld32_at<32>(lane_base + colS + 32, r);
+                tmem_ld32_at<64>(lane_base + colS + 64, r);
+                tmem_ld32_at<96>(lane_base + colS + 96, r);
+                tmem_wait_ld_fence(r);
                 if constexpr (C::kPsmem) {
-                    // this row's 128 bytes in the 128-byte swizzle the MMA reads (16-byte
-                    // granule g of row r at g ^ (r % 8)), then visible to the tensor core
-                    const uint32_t prow = smem_base + C::kOffP + t * C::kPBytes + row_in_tile * 128;
-#pragma unroll
-                    for (int g = 0; g < 8; ++g)
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + ((g ^ (row_in_tile & 7)) * 16)),
-                                     "r"(pk[4 * g]), "r"(pk[4 * g + 1]), "r"(pk[4 * g + 2]), "r"(pk[4 * g + 3])
-                                     : "memory");
-                    fence_proxy_async_smem();
-                } else {
-                    tmem_st32(lane_base + colS, pk);
+                    // S_t(j) is in registers: its columns may take S_t(j+1)
+                    tc_fence_before();
+                    mbar_arrive(smem_u32(&bars.s_free[t]));
                 }
-            } else {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
+
+                const int kv0 = j * kBN;
+                const int qlast = qrow + delta;  // last key this row reaches when causal
+                if ((kv0 + kBN > N_kv) || (args.causal && kv0 + kBN - 1 > qlast)) {
+                    // keys >= N_kv, and keys after this query row when causal, drop out
+                    const int valid = min(N_kv - kv0, args.causal ? qlast - kv0 + 1 : kBN);
+    #pragma unroll
+                    for (int i = 0; i < 128; ++i)
+                        if (i >= valid) r[i] = mask_bits;
+                }
+                // block max of the scaled scores = c * (max of the raw scores) for c >= 0
+                const float mt = cj * block_extreme(r, c_pos);
+                // lazy rescale: move the reference only when the block max exceeds it by > kTau
+                float alpha = 1.f;
+                const bool bump = mt > m_ref + kTau;
+                if (bump) {
+                    alpha = (m_ref == -INFINITY) ? 0.f : ex2_approx(m_ref - mt);
+                    m_ref = mt;
+                    l *= alpha;
+                }
+                const float ref = (m_ref == -INFINITY) ? 0.f : m_ref;
+                const float2 c2 = make_float2(cj, cj), nref2 = make_float2(bj - ref, bj - ref);
+                if (C::kPsmem && j > 0) {
+                    // P_t(j) replaces P_t(j-1), and O_t may be rescaled, once O_t += P_t(j-1) V
+                    // has completed
+                    ok = mbar_wait(smem_u32(&bars.pv_done[t]), (gj + j - 1) & 1, lim, &abort_flag);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    tc_fence_after();
+                }
+                float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0;
+                if (FP8) {
                     uint32_t pk[32];
-#pragma unroll
+    #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        const int e = 64 * h + 2 * i;
-                        const float2 x = __ffma2_rn(
-                            make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), c2, nref2);
-                        const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-                        if (i & 1)
-                            acc1 = __fadd2_rn(acc1, p);
-                        else
-                            acc0 = __fadd2_rn(acc0, p);
-                        pk[i] = pack_bf16x2(p.x, p.y);
+                        const float2 x01 = __ffma2_rn(
+                            make_float2(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1])), c2, nref2);
+                        const float2 x23 = __ffma2_rn(
+                            make_float2(__uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])), c2, nref2);
+                        const float2 p01 = make_float2(ex2_approx(x01.x), ex2_approx(x01.y));
+                        const float2 p23 = make_float2(ex2_approx(x23.x), ex2_approx(x23.y));
+                        acc0 = __fadd2_rn(acc0, p01);
+                        acc1 = __fadd2_rn(acc1, p23);
+                        pk[i] = pack_e4m3x4(p01.x, p01.y, p23.x, p23.y);
                     }
-                    tmem_st32(lane_base + colS + 32 * h, pk);
+                    if constexpr (C::kPsmem) {
+                        // this row's 128 bytes in the 128-byte swizzle the MMA reads (16-byte
+                        // granule g of row r at g ^ (r % 8)), then visible to the tensor core
+                        const uint32_t prow = smem_base + C::kOffP + t * C::kPBytes + row_in_tile * 128;
+    #pragma unroll
+                        for (int g = 0; g < 8; ++g)
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + ((g ^ (row_in_tile & 7)) * 16)),
+                                         "r"(pk[4 * g]), "r"(pk[4 * g + 1]), "r"(pk[4 * g + 2]), "r"(pk[4 * g + 3])
+                                         : "memory");
+                        fence_proxy_async_smem();
+                    } else {
+                        tmem_st32(lane_base + colS, pk);
+                    }
+                } else {
+    #pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t pk[32];
+    #pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const int e = 64 * h + 2 * i;
+                            const float2 x = __ffma2_rn(
+                                make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), c2, nref2);
+                            const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                            if (i & 1)
+                                acc1 = __fadd2_rn(acc1, p);
+                            else
+                                acc0 = __fadd2_rn(acc0, p);
+                            pk[i] = pack_bf16x2(p.x, p.y);
+                        }
+                        tmem_st32(lane_base + colS + 32 * h, pk);
+                    }
                 }
-            }
-            if (j > 0 && __any_sync(0xffffffffu, bump)) {
-                // O_t += P V of the previous block has completed (it precedes S_t(j) in
-                // issue order, or with P in shared memory pv_done said so above), so O_t
-                // can be rescaled in place before P_t(j) is published.
-#pragma unroll
-                for (int q4 = 0; q4 < D / 32; ++q4) {
-                    uint32_t ov[32];
-                    tmem_ld32(lane_base + colO + 32 * q4, ov);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-                    tmem_st32(lane_base + colO + 32 * q4, ov);
+                if (j > 0 && __any_sync(0xffffffffu, bump)) {
+                    // O_t += P V of the previous block has completed (it precedes S_t(j) in
+                    // issue order, or with P in shared memory pv_done said so above), so O_t
+                    // can be rescaled in place before P_t(j) is published.
+    #pragma unroll
+                    for (int q4 = 0; q4 < D / 32; ++q4) {
+                        uint32_t ov[32];
+                        tmem_ld32(lane_base + colO + 32 * q4, ov);
+    #pragma unroll
+                        for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                        tmem_st32(lane_base + colO + 32 * q4, ov);
+                    }
                 }
+                const float rs = (acc0.x + acc0.y) + (acc1.x + acc1.y);
+                l = (PB) ? fmaf(rs, inv_rj, l) : l + rs;
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(smem_u32(&bars.p_full[t]));
             }
-            const float rs = (acc0.x + acc0.y) + (acc1.x + acc1.y);
-            l = (PB) ? fmaf(rs, inv_rj, l) : l + rs;
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(smem_u32(&bars.p_full[t]));
-        }
-        if (ok && (!SHARD || n_kv > 0)) {
-            ok = mbar_wait(smem_u32(&bars.o_done[t]), 0, lim, &abort_flag);
-            ok = __all_sync(0xffffffffu, ok);
-        }
-        if (!ok) {
-            if (lane == 0) record_timeout(args.ctl, &abort_flag);
-        } else {
+            gj += n_kv;
+            if (ok && (!SHARD || n_kv > 0)) {
+                ok = mbar_wait(smem_u32(&bars.o_done[t]), kd & 1, lim, &abort_flag);
+                ok = __all_sync(0xffffffffu, ok);
+                ++kd;
+            }
+            if (!ok) {
+                if (lane == 0) record_timeout(args.ctl, &abort_flag);
+                break;
+            }
             tc_fence_after();
-            // a row that saw no key (l = 0; only in a causal key shard) gives O = 0 and
-            // lse = -inf: its O columns hold P V with P = 0, or were never written
+            // A row that saw no key (l = 0; only in a causal key shard) gives O = 0 and
+            // lse = -inf.  O_t is read before this warp publishes the next item's first P,
+            // so the next item's first P V (which overwrites O_t) comes after these loads.
             const float inv = (!SHARD || l > 0.f) ? o_scale / l : 0.f;
-            const size_t orow = (static_cast<size_t>(bh) * N + qrow) * D;
-            if constexpr (!SHARD && !FP8) {
-                // Coalesced O: each row goes into this tile's Q buffer (free: every S MMA
-                // of the tile completed before o_done) in the 128-byte swizzled layout
-                // (16-byte granule g of row r at g ^ (r % 8)); one thread then writes the
-                // tile with TMA stores of whole lines.  Rows past N are clipped by the TMA.
-                const uint32_t stage = smem_base + C::kOffQ + t * C::kTileBytes;
+            const size_t orow = (static_cast<size_t>(I.bh) * N + qrow) * D;
 #pragma unroll
-                for (int q4 = 0; q4 < D / 32; ++q4) {
-                    uint32_t ov[32];
+            for (int q4 = 0; q4 < D / 32; ++q4) {
+                uint32_t ov[32];
+                if (!SHARD || n_kv > 0) {
                     tmem_ld32(lane_base + colO + 32 * q4, ov);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) ov[i] = 0u;
+                }
+                if (SHARD && qrow < N) {
+                    float4* out = reinterpret_cast<float4*>(static_cast<float*>(args.o) + orow + 32 * q4);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        out[i] = make_float4(__uint_as_float(ov[4 * i]) * inv, __uint_as_float(ov[4 * i + 1]) * inv,
+                                             __uint_as_float(ov[4 * i + 2]) * inv, __uint_as_float(ov[4 * i + 3]) * inv);
+                } else if (qrow < N) {
                     uint32_t w[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
                         w[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv, __uint_as_float(ov[2 * i + 1]) * inv);
-                    const uint32_t rowbase = stage + (q4 >> 1) * C::kChunkBytes + row_in_tile * 128;
+                    uint4* out = reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.o) + orow + 32 * q4);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int gran = ((q4 & 1) * 4 + i) ^ (row_in_tile & 7);
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(rowbase + gran * 16),
-                                     "r"(w[4 * i]), "r"(w[4 * i + 1]), "r"(w[4 * i + 2]), "r"(w[4 * i + 3])
-                                     : "memory");
-                    }
-                }
-                fence_proxy_async_smem();  // generic-proxy writes -> visible to the TMA unit
-                mbar_arrive(smem_u32(&bars.o_staged[t]));
-                if (wq == 0 && lane == 0) {
-                    // bounded: a warp that gave up never arrives, and this wait then ends too
-                    if (mbar_wait(smem_u32(&bars.o_staged[t]), 0, lim, &abort_flag)) {
-#pragma unroll
-                        for (int c = 0; c < C::kChunks; ++c)
-                            tma_store_3d(&tm_o, stage + c * C::kChunkBytes, c * 64, r0 + t * kBM, bh);
-                        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-                        // complete before the CTA exits (its shared memory is released)
-                        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-                    } else {
-                        record_timeout(args.ctl, &abort_flag);
-                    }
-                }
-            } else {
-#pragma unroll
-                for (int q4 = 0; q4 < D / 32; ++q4) {
-                    uint32_t ov[32];
-                    if (!SHARD || n_kv > 0) {
-                        tmem_ld32(lane_base + colO + 32 * q4, ov);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) ov[i] = 0u;
-                    }
-                    if (SHARD && qrow < N) {
-                        float4* out = reinterpret_cast<float4*>(static_cast<float*>(args.o) + orow + 32 * q4);
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            out[i] = make_float4(__uint_as_float(ov[4 * i]) * inv, __uint_as_float(ov[4 * i + 1]) * inv,
-                                                 __uint_as_float(ov[4 * i + 2]) * inv, __uint_as_float(ov[4 * i + 3]) * inv);
-                    } else if (qrow < N) {
-                        uint32_t w[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            w[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv,
-                                               __uint_as_float(ov[2 * i + 1]) * inv);
-                        uint4* out = reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.o) + orow + 32 * q4);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            out[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-                    }
+                    for (int i = 0; i < 4; ++i)
+                        out[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
                 }
             }
             if (qrow < N && args.lse != nullptr)
-                args.lse[static_cast<size_t>(bh) * N + qrow] = (m_ref + log2f(l)) * 0.69314718055994530942f;
+                args.lse[static_cast<size_t>(I.bh) * N + qrow] = (m_ref + log2f(l)) * 0.69314718055994530942f;
         }
     }
 
@@ -709,10 +744,6 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse
     int rc = make_map_3d(&tq, q, dt, C::kElem, D, N, BH, C::kBoxX, kBM);
     if (rc == 0) rc = make_map_3d(&tk, k, dt, C::kElem, D, N_kv, BH_kv, C::kBoxX, kBN);
     if (rc == 0) rc = make_map_3d(&tv, v, dt, C::kElem, D, N_kv, BH_kv, C::kBoxX, kBN);
-    // O [BH][N][D] bf16, written in (64 x 128) boxes (bf16 outputs only)
-    CUtensorMap to = tq;
-    if (rc == 0 && !SHARD && !FP8)
-        rc = make_map_3d(&to, o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, N, BH, 64, kBM);
     if (rc != 0) return rc;
     static uint64_t attr_set = 0;  // per template instance, one bit per device
     int dev = 0;
@@ -748,8 +779,16 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse
     a.qk_descale_k = kd;
     a.v_descale = vd;
     a.ctl = ctl;
-    return static_cast<int>(launch_pdl(fwd_sm103_kernel<D, FP8, SHARD, PB>, dim3(a.n_pairs * BH),
-                                       dim3(kThreads), C::kSmemAlloc, s, tq, tk, tv, to, a));
+    // bf16: persistent, one CTA per SM (fewer if there are fewer items), each looping over
+    // items.  E4M3: one CTA per item (its k-th item is then blockIdx.x alone), placed by the
+    // hardware as SMs free up: its items are short, and dealing them statically measured
+    // 4-8% slower than letting the next CTA take the first free SM.
+    int sms = 152;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int n_items = a.n_pairs * BH;
+    const int grid = (FP8 || n_items < sms) ? n_items : sms;
+    return static_cast<int>(launch_pdl(fwd_sm103_kernel<D, FP8, SHARD, PB>, dim3(grid), dim3(kThreads),
+                                       C::kSmemAlloc, s, tq, tk, tv, a));
 }
 
 }  // namespace
