@@ -114,6 +114,28 @@ def test_bf16_config_b1_h32_n16384_d128_sampled(causal):
         assert max_err(o_c[0, :, 0], f64(x["v"][0, :, 0])) <= 1e-2
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_many_heads_ragged_n_every_head(d, causal):
+    # Many more (head, query-tile pair) items than SMs, each with a ragged last tile
+    # (N = 1000: four pairs, the last one 232 rows): every CTA of the forward works
+    # through several items, carrying its TMEM, barriers and K/V ring from one to the
+    # next, and items of different lengths (causal) follow each other.  Every head's
+    # tile edges and random rows against the oracle.
+    B, H, N = 2, 96, 1000
+    x, dev = device_inputs(B, H, N, d, "bf16")
+    s = scale_for(d)
+    o, lse = run_fwd(dev, fa.FA_BF16, s, causal)
+    o_c, lse_c = f64(o), f64(lse)
+    for b in range(B):
+        for h in range(H):
+            rows = head_rows(N, b * H + h, n_random=2)
+            o_ref, lse_ref = oracle.attn_fwd_rows(f64(x["q"][b, h]), f64(x["k"][b, h]),
+                                                  f64(x["v"][b, h]), rows, s, causal)
+            assert max_err(o_c[b, h, rows], o_ref) <= TOL_BF16_O, f"batch {b} head {h}"
+            assert max_err(lse_c[b, h, rows], lse_ref) <= TOL_LSE_BF16, f"batch {b} head {h}"
+
+
 def test_bf16_deterministic_and_lse_optional():
     x, dev = device_inputs(1, 2, 700, 128, "bf16")
     s = scale_for(128)
