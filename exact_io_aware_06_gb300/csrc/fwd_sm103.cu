@@ -17,8 +17,8 @@
 //     item (the next item's Q and K/V load while one finishes); E4M3: one CTA per item.
 //     O is written by each softmax thread as its row; lse likewise.
 //   * 12 warps:
-//       warp 0      TMA producer: Q once, then V_j and K_{j+1} as one bundle on one
-//                   barrier into 2-stage rings
+//       warp 0      TMA producer: each item's Q, then V_j and K_{j+1} as one bundle on
+//                   one barrier into 2-slot rings
 //       warp 1      MMA issuer (one thread) + TMEM owner
 //       warps 4-7   softmax for query tile 0, warps 8-11 for query tile 1
 //   * TMEM (512 columns): S_t (128 fp32 columns per tile), O_t (d columns);
