@@ -44,6 +44,28 @@ def test_gqa_forward(H, H_kv, N, d, causal):
     assert max_err(f64(lse), lse_ref) <= TOL_LSE_BF16
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_gqa_forward_many_items_every_head(causal):
+    # 384 (query head, tile pair) items on at most one CTA per SM: every CTA works through
+    # several items and must map each one's query head to its K/V head itself
+    B, H, H_kv, N, d = 2, 48, 6, 1000, 128
+    q, k, v = gqa_inputs(B, H, H_kv, N, d, seed=3)
+    s = scale_for(d)
+    o = torch.empty_like(q).cuda()
+    lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    fa.fa_fwd_gqa(q.cuda(), k.cuda(), v.cuda(), o, lse, s, causal, fa.FA_BF16)
+    check_status()
+    o_c, lse_c = f64(o), f64(lse)
+    rep = H // H_kv
+    for b in range(B):
+        for h in range(H):
+            rows = head_rows(N, b * H + h, n_random=2)
+            o_ref, lse_ref = oracle.attn_fwd_rows(f64(q[b, h]), f64(k[b, h // rep]), f64(v[b, h // rep]),
+                                                  rows, s, causal)
+            assert max_err(o_c[b, h, rows], o_ref) <= TOL_BF16_O, f"batch {b} head {h}"
+            assert max_err(lse_c[b, h, rows], lse_ref) <= TOL_LSE_BF16, f"batch {b} head {h}"
+
+
 def test_gqa_equals_plain_forward_with_repeated_heads():
     # same arithmetic as fa_fwd on explicitly repeated K/V: identical bits
     B, H, H_kv, N, d = 1, 8, 2, 700, 128
