@@ -53,7 +53,7 @@ extern "C" __attribute__((visibility("default"))) int fa_bwd_noalloc(
     using namespace fa;
     if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
     // B*H is formed only within the bounds fa_bwd enforces, so it cannot overflow
-    if (static_cast<int64_t>(B) * H > (1ll << 24) || N > (1 << 24)) return FA_ERR_UNSUPPORTED;
+    if (!sizes_supported(B, H, N)) return FA_ERR_UNSUPPORTED;
     // the sizes this scratch array cannot hold are refused before anything runs
     if (bwd_workspace_bytes(B * H, N, d) > kNoAllocScratchBytes) return FA_ERR_UNSUPPORTED;
     void* scratch = scratch_address();

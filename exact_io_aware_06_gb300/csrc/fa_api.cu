@@ -46,7 +46,7 @@ int check_common(const void* q, const void* k, const void* v, const void* o, con
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FA_ERR_INVALID_ARG;
     if (lse != nullptr && !aligned16(lse)) return FA_ERR_INVALID_ARG;
     if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
-    if (static_cast<int64_t>(B) * H > (1ll << 24) || N > (1 << 24)) return FA_ERR_UNSUPPORTED;
+    if (!sizes_supported(B, H, N)) return FA_ERR_UNSUPPORTED;
     return FA_OK;
 }
 
@@ -248,7 +248,7 @@ __attribute__((visibility("default"))) size_t fa_bwd_workspace_size(int B, int H
     // the product B*H is formed only once it is known to fit (the same bounds the
     // backward itself enforces); sizes outside them have no workspace
     if (B < 1 || H < 1 || N < 1 || d < 1) return 0;
-    if (static_cast<int64_t>(B) * H > (1ll << 24) || N > (1 << 24)) return 0;
+    if (!sizes_supported(B, H, N)) return 0;
     return bwd_workspace_bytes(B * H, N, d);
 }
 

@@ -16,6 +16,14 @@ constexpr int kDevTimeout = 4;  // == FA_ERR_DEVICE_TIMEOUT
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;
 constexpr uint64_t kDrainWaitNs = 1000000000ull;
 
+// Sizes every entry point accepts: B*H heads and N rows each at most 2^24, and the
+// kernels' work items -- (head, 128-row block) for the backward, (head, 256-row pair) for
+// the forward -- countable in an int (B*H*ceil(N/128) <= 2^31 - 1).
+inline bool sizes_supported(int B, int H, int N) {
+    if (static_cast<int64_t>(B) * H > (1ll << 24) || N > (1 << 24)) return false;
+    return static_cast<int64_t>(B) * H * ((static_cast<int64_t>(N) + 127) / 128) <= 0x7fffffffll;
+}
+
 struct DevCtl {
     int* status;       // per-device status word (first error wins)
     uint64_t wait_ns;  // bound on one wait

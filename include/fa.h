@@ -56,6 +56,13 @@ typedef enum {
 } fa_status;
 
 /*
+ * Size limits shared by every entry point: B*H (heads, or query heads) at most
+ * 2^24, N (rows of one head) at most 2^24, and B*H*ceil(N/128) at most 2^31 - 1,
+ * so that the kernels' work items (128-row blocks of one head) can be counted in
+ * an int.  Larger sizes are refused with FA_ERR_UNSUPPORTED before anything runs.
+ */
+
+/*
  * Forward pass.  O = softmax(scale Q K^T [causal mask]) V and
  * lse_i = m_i + ln l_i (natural log, in units of the scaled score; m_i the row
  * max, l_i the row sum of exp(S_ij - m_i)), as on the "FlashAttention-1" page
@@ -190,8 +197,8 @@ int fa_lse_merge(const float* o_parts, const float* lse_parts, int n_parts, void
  * delta_i = dO_i . O_i and the pre-scaled lse (float32, N rounded up to 128
  * per head), plus for d = 64 the float32 dQ accumulator
  * ([B][H][N rounded up to 128][d]).
- * Returns 0 for invalid sizes and for sizes the backward refuses
- * (B*H > 2^24 or N > 2^24), whose byte count could overflow.
+ * Returns 0 for invalid sizes and for sizes the backward refuses (beyond the
+ * size limits above), whose byte count could overflow.
  */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 

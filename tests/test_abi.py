@@ -88,6 +88,22 @@ def test_fwd_argument_errors(L):
     assert fwd(L, d=256) == 2
 
 
+def test_size_limits(L):
+    # B*H and N each at most 2^24, and B*H*ceil(N/128) work items at most 2^31 - 1
+    assert fwd(L, B=1 << 12, H=1 << 13) == 2            # B*H = 2^25
+    assert fwd(L, N=(1 << 24) + 1) == 2
+    assert fwd(L, B=1 << 12, H=1 << 12, N=1 << 24) == 2  # 2^24 heads x 2^17 blocks
+    assert fwd(L, B=1 << 8, H=1 << 8, N=1 << 22) == 2    # exactly 2^31 blocks
+    # the workspace query applies the same limits, at the boundary on both sides
+    assert fa.fa_bwd_workspace_size(1 << 8, 1 << 8, 1 << 22, 128) == 0
+    ok = fa.fa_bwd_workspace_size(1 << 8, 1 << 8, (1 << 22) - 128, 128)
+    assert ok == 2 * (1 << 16) * ((1 << 22) - 128) * 4
+    assert fa.fa_bwd_workspace_size(1, 1, (1 << 24) + 1, 64) == 0
+    # the allocation-free backward refuses them before looking at its scratch
+    assert L.fa_bwd_noalloc(P, P, P, P, P, P, P, P, P, 1 << 8, 1 << 8, 1 << 22, 64, 0.125, 0,
+                            1, None) == 2
+
+
 def test_fp8_argument_errors(L):
     def f(qd=1.0, d=128, N=128):
         return L.fa_fwd_fp8(P, P, P, P, None, qd, 1.0, 1.0, 1, 1, N, d, 0.1, 0, None)
