@@ -38,6 +38,12 @@
 //     block max exceeds it by more than kTau (log2 units).  O and l always share
 //     the same reference, so the result is exact for any threshold; p stays
 //     <= 2^kTau (fine for bf16 and below the E4M3 limit of 448).
+//   * Solo items (bf16): when the last round of pairs would leave SMs idle, its pairs are
+//     dealt as single 128-row tiles, and a pair whose second tile lies past N runs as its
+//     first tile alone.  Both softmax warpgroups then hold the tile's rows and take
+//     alternate key blocks (warpgroup t the blocks t, t+2, ...), each with its own running
+//     max, sum and O_t; warpgroup 0 merges the two halves at the end with the two-state
+//     combination of the "FlashAttention-1" page (10.2.2).
 //   * Every wait is bounded; on a timeout the kernel records it, drains its own
 //     TMA loads and MMAs, frees TMEM and exits.
 #include <cmath>
@@ -64,7 +70,8 @@ struct FwdArgs {
     int delta;        // causal: key j reaches query i iff j <= i + delta (0 unless sharded)
     int n_pairs;      // query-tile pairs per head
     int BH;           // query heads (B * H)
-    int hgrp;         // causal: heads per scheduling group (see the tile mapping)
+    int n_items;      // work items: n_pair_items pairs, then single tiles (solo items)
+    int n_pair_items; // items dealt as whole pairs; pair n_pair_items + s/2 gives solo s
     float c_log2;     // scale * log2(e) (times the FP8 descales)
     float o_scale;    // multiplies O at the end (FP8: v descale), 1 otherwise
     int causal;
@@ -113,6 +120,8 @@ struct Bars {
     uint64_t kv_full[kStages], kv_empty[kStages];  // ring slot u: bundles n, n % kStages == u
     uint64_t s_full[2], p_full[2], o_done[2];
     uint64_t s_free[2], pv_done[2];  // kPsmem: S_t read out of TMEM; O_t += P_t V done
+    uint64_t merge_ml;    // solo item: warpgroup 1's running max and sum are in shared memory
+    uint64_t merge_done;  // solo item: warpgroup 0 has read O_1 (which may then be overwritten)
     uint64_t drain;
 };
 
@@ -195,8 +204,10 @@ __device__ __forceinline__ float block_extreme(const uint32_t (&r)[128], bool wa
 // q_free, o_done), per K/V block (s_full, p_full, s_free, pv_done) or per bundle
 // (kv_full, kv_empty), so TMEM, the barriers and the K/V ring carry over from one item to
 // the next, and the next item's Q and first bundle load while this item finishes.  An
-// item whose queries see no key (only in a causal key shard) involves neither the
-// producer nor the MMA thread: the softmax warps write its O = 0 and lse = -inf.
+// item whose queries see no key (in a causal key shard; or a solo tile past N) involves
+// neither the producer nor the MMA thread: the softmax warps write its O = 0 and lse = -inf
+// (the solo tile has no rows to write).  Per-tile barriers count each tile's own blocks,
+// since a solo item gives the two tiles different numbers of blocks.
 template <int D, bool FP8, bool SHARD, bool PB = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -206,6 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ __align__(8) Bars bars;
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
+    __shared__ float merge_m[kBM], merge_l[kBM];  // solo item: warpgroup 1's max and sum per row
 
     const uint32_t smem_base =
         (smem_u32(smem_raw) + 1023u) & ~1023u;  // 1 KB aligned for the 128 B swizzle
@@ -213,12 +225,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int N = args.N;
     const int N_kv = SHARD ? args.N_kv : N;
     const int delta = SHARD ? args.delta : 0;
-    const int n_items = args.n_pairs * args.BH;
+    const int n_items = args.n_items;
     const int G = static_cast<int>(gridDim.x);
     // E4M3 runs one CTA per item (see the launch); with a compile-time single pass every
     // running counter below is a constant there
     constexpr bool kPersist = !FP8;
     constexpr int kItemsMax = kPersist ? 0x7fffffff : 1;
+    constexpr bool kSolo = !FP8 && !SHARD;  // single-tile items (E4M3 and shards: pairs only)
 
     // this CTA's k-th item, dealt in alternating (snake) order so that no CTA always
     // takes the heaviest item of a round (causal items are ordered heaviest first)
@@ -227,34 +240,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     struct Item {
         int bh, bh_kv, r0, n_kv;
+        bool solo;  // one query tile (rows r0 .. r0 + 127), not two
     };
-    // Item x's tile pair.  Non-causal: head-major, every pair of a head together (the
-    // head's K/V stays in L2).  Causal: a pair's work grows with its index, so items run
-    // heaviest pair first across a group of hgrp heads (whose K/V fits in L2), group
-    // after group; head-major order would leave the last heads' heaviest pairs for the
-    // end and a long tail.
+    // Item x's tiles.  Items below n_pair_items are pairs in the order below; the rest
+    // are single tiles, solo item s being tile s % 2 of pair n_pair_items + s / 2.
+    // Pair order, non-causal: head-major, every pair of a head together (the head's K/V
+    // stays in L2).  Causal: a pair's work grows with its index, so items run heaviest pair
+    // first across all heads, which with the alternating deal keeps the CTAs' loads within
+    // a few blocks of each other.  (Head-major order leaves the last heads' heaviest pairs
+    // for the end; heaviest first within groups of heads whose K/V fits in L2 kept K/V in L2
+    // but left the loads 4-14% apart, and measured 0.4-11% slower.)
     auto item_at = [&](int x) {
+        int p = x, tile = 0;
+        bool solo = false;
+        if (kSolo && x >= args.n_pair_items) {
+            p = args.n_pair_items + (x - args.n_pair_items) / 2;
+            tile = (x - args.n_pair_items) & 1;
+            solo = true;
+        }
         int bh, pair;
         if (args.causal) {
-            const int span = args.hgrp * args.n_pairs;
-            const int grp = x / span;
-            const int hg = min(args.hgrp, args.BH - grp * args.hgrp);  // heads in this group
-            const int xi = x - grp * span;
-            pair = args.n_pairs - 1 - xi / hg;
-            bh = grp * args.hgrp + xi % hg;
+            pair = args.n_pairs - 1 - p / args.BH;
+            bh = p % args.BH;
         } else {
-            bh = x / args.n_pairs;
-            pair = args.n_pairs - 1 - (x % args.n_pairs);
+            bh = p / args.n_pairs;
+            pair = args.n_pairs - 1 - (p % args.n_pairs);
         }
         Item I;
         I.bh = bh;
         // grouped-query attention: H / H_kv query heads share one K/V head
         I.bh_kv = (bh / args.H) * args.H_kv + (bh % args.H) / (args.H / args.H_kv);
-        I.r0 = pair * 2 * kBM;
-        // keys this pair of tiles can see; none at all when a causal key shard lies
-        // wholly after these queries
-        const int kv_end = args.causal ? min(N_kv, I.r0 + 2 * kBM + delta) : N_kv;
-        I.n_kv = (!SHARD || kv_end > 0) ? (kv_end + kBN - 1) / kBN : 0;
+        I.r0 = pair * 2 * kBM + tile * kBM;
+        // a pair whose second tile lies wholly past N is its first tile alone
+        if (kSolo && !solo && I.r0 + kBM >= N) solo = true;
+        I.solo = solo;
+        // keys these query rows can see; none at all when a causal key shard lies wholly
+        // after them, or for a solo tile past N
+        const int kv_end = args.causal ? min(N_kv, I.r0 + (solo ? kBM : 2 * kBM) + delta) : N_kv;
+        I.n_kv = (I.r0 < N && (!SHARD || kv_end > 0)) ? (kv_end + kBN - 1) / kBN : 0;
         return I;
     };
 
@@ -273,6 +296,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&bars.s_free[t]), 128);
             mbar_init(smem_u32(&bars.pv_done[t]), 1);
         }
+        mbar_init(smem_u32(&bars.merge_ml), 128);
+        mbar_init(smem_u32(&bars.merge_done), 128);
         mbar_init(smem_u32(&bars.drain), 1);
         fence_barrier_init();
     }
@@ -311,14 +336,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int x = item_x(k);
                 if (x >= n_items) break;
                 const Item I = item_at(x);
-                if (SHARD && I.n_kv == 0) continue;
+                if (I.n_kv == 0) continue;
                 // Q of this item once the last S MMAs of the previous one have read the Q buffers
                 if (kq > 0 && !mbar_wait(smem_u32(&bars.q_free), (kq - 1) & 1, lim, &abort_flag)) {
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(qf, 2 * C::kTileBytes);
-                for (int t = 0; t < 2; ++t)
+                const int n_q = I.solo ? 1 : 2;
+                mbar_arrive_expect_tx(qf, n_q * C::kTileBytes);
+                for (int t = 0; t < n_q; ++t)
                     for (int c = 0; c < C::kChunks; ++c)
                         tma_load_3d(smem_base + C::kOffQ + t * C::kTileBytes + c * C::kChunkBytes, &tm_q,
                                     qf, c * C::kBoxX, I.r0 + t * kBM, I.bh);
@@ -398,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             };
             int gb = 0;  // bundle index of the current item's bundle 0, over all items
-            int gj = 0;  // index of the current item's first K/V block, over all items
+            int c0 = 0, c1 = 0;  // K/V blocks of tile 0 / tile 1 before the current item
             bool ok = true;
             // One K/V block j of the current item.  MORE (compile-time): a block j+1 follows,
             // so S_t(j+1) is issued; otherwise o_done is committed.  LAST2: block j+1 is the
@@ -409,38 +435,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             //  - E4M3 (kPsmem): S_0(j+1) and S_1(j+1) as soon as the softmax warps have read
             //    S_t(j) out of TMEM, then O_t += P_t(j) V_j as each P_t(j) is published; the
             //    bundle is released after P_1(j) V_j.
-            // g1: index of bundle j+1 over all items; pj: parity of block j's per-block barriers
-            // (both passed by value, so the running counters stay out of the loop body)
-            auto block = [&](int j, int g1, uint32_t pj, auto more_c, auto last2_c) -> bool {
+            // g1: index of bundle j+1 over all items; p0, p1: parity of block j's per-block
+            // barriers of tile 0 and tile 1 (passed by value, so the running counters stay out
+            // of the loop body)
+            auto block = [&](int j, int g1, uint32_t p0, uint32_t p1, auto more_c, auto last2_c) -> bool {
                 constexpr bool more = decltype(more_c)::value, last2 = decltype(last2_c)::value;
                 const int u = g1 % kStages;
                 const uint32_t phu = (g1 / kStages) & 1;
                 if constexpr (C::kPsmem) {
                     if (!mbar_wait(smem_u32(&bars.kv_full[u]), phu, lim, &abort_flag)) return false;
                     if constexpr (more) {
-                        if (!mbar_wait(smem_u32(&bars.s_free[0]), pj, lim, &abort_flag)) return false;
+                        if (!mbar_wait(smem_u32(&bars.s_free[0]), p0, lim, &abort_flag)) return false;
                         tc_fence_after();
                         issue_s(q_lo0, u, C::kColS0);
                         mma_commit(smem_u32(&bars.s_full[0]));
-                        if (!mbar_wait(smem_u32(&bars.s_free[1]), pj, lim, &abort_flag)) return false;
+                        if (!mbar_wait(smem_u32(&bars.s_free[1]), p1, lim, &abort_flag)) return false;
                         tc_fence_after();
                         issue_s(q_lo1, u, C::kColS1);
                         mma_commit(smem_u32(&bars.s_full[1]));
                         if constexpr (last2) mma_commit(smem_u32(&bars.q_free));
                     }
-                    if (!mbar_wait(smem_u32(&bars.p_full[0]), pj, lim, &abort_flag)) return false;
+                    if (!mbar_wait(smem_u32(&bars.p_full[0]), p0, lim, &abort_flag)) return false;
                     tc_fence_after();
                     issue_pv_s(p_lo0, u, C::kColO0, j > 0);
                     mma_commit(smem_u32(&bars.pv_done[0]));
                     if constexpr (!more) mma_commit(smem_u32(&bars.o_done[0]));
-                    if (!mbar_wait(smem_u32(&bars.p_full[1]), pj, lim, &abort_flag)) return false;
+                    if (!mbar_wait(smem_u32(&bars.p_full[1]), p1, lim, &abort_flag)) return false;
                     tc_fence_after();
                     issue_pv_s(p_lo0 + (C::kPBytes >> 4), u, C::kColO1, j > 0);
                     mma_commit(smem_u32(&bars.pv_done[1]));
                     if constexpr (!more) mma_commit(smem_u32(&bars.o_done[1]));
                 } else {
                     if (!mbar_wait(smem_u32(&bars.kv_full[u]), phu, lim, &abort_flag)) return false;
-                    if (!mbar_wait(smem_u32(&bars.p_full[0]), pj, lim, &abort_flag)) return false;
+                    if (!mbar_wait(smem_u32(&bars.p_full[0]), p0, lim, &abort_flag)) return false;
                     tc_fence_after();
                     issue_pv(C::kColS0, u, C::kColO0, j > 0);
                     if constexpr (more) {
@@ -449,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     } else {
                         mma_commit(smem_u32(&bars.o_done[0]));
                     }
-                    if (!mbar_wait(smem_u32(&bars.p_full[1]), pj, lim, &abort_flag)) return false;
+                    if (!mbar_wait(smem_u32(&bars.p_full[1]), p1, lim, &abort_flag)) return false;
                     tc_fence_after();
                     issue_pv(C::kColS1, u, C::kColO1, j > 0);
                     if constexpr (more) {
@@ -470,31 +497,65 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int x = item_x(k);
                 if (x >= n_items) break;
                 const Item I = item_at(x);
-                if (SHARD && I.n_kv == 0) continue;  // no key reaches these queries
+                if (I.n_kv == 0) continue;  // no key reaches these queries
                 ok = mbar_wait(smem_u32(&bars.q_full), kq & 1, lim, &abort_flag);
                 if (!ok) break;
                 // the item's first scores: bundle 0 holds K_0; with P in shared memory the
                 // previous item's last S_t must have been read out of TMEM first
                 ok = mbar_wait(smem_u32(&bars.kv_full[gb % kStages]), (gb / kStages) & 1, lim, &abort_flag);
-                if (ok && C::kPsmem && gj > 0) {
-                    ok = mbar_wait(smem_u32(&bars.s_free[0]), (gj - 1) & 1, lim, &abort_flag);
-                    if (ok) ok = mbar_wait(smem_u32(&bars.s_free[1]), (gj - 1) & 1, lim, &abort_flag);
+                if (ok && C::kPsmem && c0 > 0) {
+                    ok = mbar_wait(smem_u32(&bars.s_free[0]), (c0 - 1) & 1, lim, &abort_flag);
+                    if (ok) ok = mbar_wait(smem_u32(&bars.s_free[1]), (c1 - 1) & 1, lim, &abort_flag);
                 }
                 if (!ok) break;
                 tc_fence_after();
-                issue_s(q_lo0, gb % kStages, C::kColS0);
-                mma_commit(smem_u32(&bars.s_full[0]));
-                issue_s(q_lo1, gb % kStages, C::kColS1);
-                mma_commit(smem_u32(&bars.s_full[1]));
-                if (I.n_kv == 1) mma_commit(smem_u32(&bars.q_free));
-                mma_commit(smem_u32(&bars.kv_empty[gb % kStages]));  // bundle 0 read
-                const int g0 = gb, j0 = gj;
-                int j = 0;
-                for (; j + 2 < I.n_kv && ok; ++j) ok = block(j, g0 + j + 1, (j0 + j) & 1, T{}, F{});
-                if (ok && I.n_kv >= 2) ok = block(I.n_kv - 2, g0 + I.n_kv - 1, (j0 + I.n_kv - 2) & 1, T{}, T{});
-                if (ok) ok = block(I.n_kv - 1, g0 + I.n_kv, (j0 + I.n_kv - 1) & 1, F{}, F{});
+                if (kSolo && I.solo) {
+                    // One query tile (Q_0); key block b belongs to softmax warpgroup b % 2, whose
+                    // S, P and O columns it uses.  Bundle n = {K_n, V_{n-1}}: first S_{n%2}(n)
+                    // (those columns held P(n-2), whose P V went out with the previous bundle and
+                    // runs first), then P(n-1) V_{n-1} once warpgroup (n-1) % 2 has published it.
+                    const int u0 = gb % kStages;
+                    issue_s(q_lo0, u0, C::kColS0);
+                    mma_commit(smem_u32(&bars.s_full[0]));
+                    if (I.n_kv == 1) mma_commit(smem_u32(&bars.q_free));
+                    mma_commit(smem_u32(&bars.kv_empty[u0]));  // bundle 0 read
+                    for (int n = 1; ok && n <= I.n_kv; ++n) {
+                        const int g = gb + n, u = g % kStages;
+                        ok = mbar_wait(smem_u32(&bars.kv_full[u]), (g / kStages) & 1, lim, &abort_flag);
+                        if (!ok) break;
+                        tc_fence_after();
+                        if (n < I.n_kv) {
+                            const int ts = n & 1;
+                            issue_s(q_lo0, u, ts ? C::kColS1 : C::kColS0);
+                            mma_commit(smem_u32(&bars.s_full[ts]));
+                            if (n == I.n_kv - 1) mma_commit(smem_u32(&bars.q_free));
+                        }
+                        const int b = n - 1, tb = b & 1;
+                        ok = mbar_wait(smem_u32(&bars.p_full[tb]), ((tb ? c1 : c0) + b / 2) & 1, lim, &abort_flag);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_pv(tb ? C::kColS1 : C::kColS0, u, tb ? C::kColO1 : C::kColO0, b >= 2);
+                        if (b + 2 >= I.n_kv) mma_commit(smem_u32(&bars.o_done[tb]));  // tile tb's last
+                        mma_commit(smem_u32(&bars.kv_empty[u]));  // bundle n read
+                    }
+                    c0 += (I.n_kv + 1) / 2;
+                    c1 += I.n_kv / 2;
+                } else {
+                    issue_s(q_lo0, gb % kStages, C::kColS0);
+                    mma_commit(smem_u32(&bars.s_full[0]));
+                    issue_s(q_lo1, gb % kStages, C::kColS1);
+                    mma_commit(smem_u32(&bars.s_full[1]));
+                    if (I.n_kv == 1) mma_commit(smem_u32(&bars.q_free));
+                    mma_commit(smem_u32(&bars.kv_empty[gb % kStages]));  // bundle 0 read
+                    const int g0 = gb, a0 = c0, a1 = c1, n = I.n_kv;
+                    int j = 0;
+                    for (; j + 2 < n && ok; ++j) ok = block(j, g0 + j + 1, (a0 + j) & 1, (a1 + j) & 1, T{}, F{});
+                    if (ok && n >= 2) ok = block(n - 2, g0 + n - 1, (a0 + n - 2) & 1, (a1 + n - 2) & 1, T{}, T{});
+                    if (ok) ok = block(n - 1, g0 + n, (a0 + n - 1) & 1, (a1 + n - 1) & 1, F{}, F{});
+                    c0 += n;
+                    c1 += n;
+                }
                 gb += I.n_kv + 1;
-                gj += I.n_kv;
                 ++kq;
             }
             if (!ok) record_timeout(args.ctl, &abort_flag);
@@ -514,15 +575,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
         const uint32_t colS = t ? C::kColS1 : C::kColS0;
         const uint32_t colO = t ? C::kColO1 : C::kColO0;
-        int gj = 0;  // index of the current item's first K/V block, over all items
-        int kd = 0;  // items with at least one key block done
+        int gj = 0;  // K/V blocks this warpgroup processed before the current item
+        int kd = 0;  // items in which this warpgroup processed at least one key block
+        int ns = 0;  // solo items merged
         bool ok = true;
         for (int k = 0; ok && k < kItemsMax; ++k) {
             const int x = item_x(k);
             if (x >= n_items) break;
             const Item I = item_at(x);
             const int n_kv = I.n_kv;
-            const int qrow = I.r0 + t * kBM + row_in_tile;
+            // solo item: both warpgroups hold the tile's rows, warpgroup t taking key blocks
+            // t, t + 2, ...; a solo tile past N has no rows and no keys
+            const bool solo = kSolo && I.solo;
+            if (solo && n_kv == 0) continue;
+            const int tile_r0 = I.r0 + (solo ? 0 : t * kBM);
+            const int qrow = tile_r0 + row_in_tile;
             // per-head FP8 descales fold into the score constant and the output scale
             float c = args.c_log2, o_scale = args.o_scale;
             // per-block FP8 descales: this tile's Q factor folds into c, key block j's K factor
@@ -537,7 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float lg_vmax = 0.f;
             if (PB) {
                 const int n_kb = (N_kv + kBN - 1) / kBN;
-                c *= args.qk_descale_q[static_cast<size_t>(I.bh) * ((N + kBM - 1) / kBM) + (I.r0 / kBM + t)];
+                c *= args.qk_descale_q[static_cast<size_t>(I.bh) * ((N + kBM - 1) / kBM) + tile_r0 / kBM];
                 kd_blk = args.qk_descale_k + static_cast<size_t>(I.bh_kv) * n_kb;
                 vd_blk = args.v_descale + static_cast<size_t>(I.bh_kv) * n_kb;
                 float vm = 0.f;
@@ -556,7 +623,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             float m_ref = -INFINITY;  // reference max in log2 units
             float l = 0.f;
 
-            for (int j = 0; j < n_kv; ++j) {
+            int i = 0;  // key blocks of this item done by this warpgroup
+            for (int j = solo ? t : 0; j < n_kv; j += solo ? 2 : 1, ++i) {
                 // key block j's factors (per-block FP8), loaded before the wait
                 float cj = c, bj = 0.f, inv_rj = 1.f;
                 if (PB) {
@@ -565,7 +633,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     bj = fmaxf(lg2_approx(vdj) - lg_vmax, -100.f);
                     inv_rj = ex2_approx(-bj);
                 }
-                ok = mbar_wait(smem_u32(&bars.s_full[t]), (gj + j) & 1, lim, &abort_flag);
+                ok = mbar_wait(smem_u32(&bars.s_full[t]), (gj + i) & 1, lim, &abort_flag);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();
@@ -602,10 +670,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const float ref = (m_ref == -INFINITY) ? 0.f : m_ref;
                 const float2 c2 = make_float2(cj, cj), nref2 = make_float2(bj - ref, bj - ref);
-                if (C::kPsmem && j > 0) {
+                if (C::kPsmem && i > 0) {
                     // P_t(j) replaces P_t(j-1), and O_t may be rescaled, once O_t += P_t(j-1) V
                     // has completed
-                    ok = mbar_wait(smem_u32(&bars.pv_done[t]), (gj + j - 1) & 1, lim, &abort_flag);
+                    ok = mbar_wait(smem_u32(&bars.pv_done[t]), (gj + i - 1) & 1, lim, &abort_flag);
                     ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
                     tc_fence_after();
@@ -657,10 +725,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_st32(lane_base + colS + 32 * h, pk);
                     }
                 }
-                if (j > 0 && __any_sync(0xffffffffu, bump)) {
-                    // O_t += P V of the previous block has completed (it precedes S_t(j) in
-                    // issue order, or with P in shared memory pv_done said so above), so O_t
-                    // can be rescaled in place before P_t(j) is published.
+                if (i > 0 && __any_sync(0xffffffffu, bump)) {
+                    // O_t += P V of this warpgroup's previous block has completed (it precedes
+                    // S_t(j) in issue order, or with P in shared memory pv_done said so above),
+                    // so O_t can be rescaled in place before P_t(j) is published.
     #pragma unroll
                     for (int q4 = 0; q4 < D / 32; ++q4) {
                         uint32_t ov[32];
@@ -676,8 +744,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 mbar_arrive(smem_u32(&bars.p_full[t]));
             }
-            gj += n_kv;
-            if (ok && (!SHARD || n_kv > 0)) {
+            gj += i;
+            if (ok && i > 0) {
                 ok = mbar_wait(smem_u32(&bars.o_done[t]), kd & 1, lim, &abort_flag);
                 ok = __all_sync(0xffffffffu, ok);
                 ++kd;
@@ -687,6 +755,70 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
+            if (solo) {
+                // Two states over disjoint key sets, each relative to its own reference max:
+                // (m_0, l_0, O_0) and (m_1, l_1, O_1).  Combined: m = max(m_0, m_1),
+                // l = 2^(m_0 - m) l_0 + 2^(m_1 - m) l_1, O = (2^(m_0 - m) O_0 + 2^(m_1 - m) O_1) / l.
+                if (t == 1) {
+                    merge_m[row_in_tile] = m_ref;
+                    merge_l[row_in_tile] = l;
+                    mbar_arrive(smem_u32(&bars.merge_ml));
+                    // O_1 stays in TMEM until warpgroup 0 has read it
+                    ok = mbar_wait(smem_u32(&bars.merge_done), ns & 1, lim, &abort_flag);
+                    ok = __all_sync(0xffffffffu, ok);
+                    ++ns;
+                    if (!ok) {
+                        if (lane == 0) record_timeout(args.ctl, &abort_flag);
+                        break;
+                    }
+                    continue;
+                }
+                ok = mbar_wait(smem_u32(&bars.merge_ml), ns & 1, lim, &abort_flag);
+                ok = __all_sync(0xffffffffu, ok);
+                ++ns;
+                if (!ok) {
+                    if (lane == 0) record_timeout(args.ctl, &abort_flag);
+                    break;
+                }
+                tc_fence_after();
+                const float m1 = merge_m[row_in_tile], l1 = merge_l[row_in_tile];
+                const float mm = fmaxf(m_ref, m1);
+                const float a0 = (m_ref == -INFINITY) ? 0.f : ex2_approx(m_ref - mm);
+                const float a1 = (m1 == -INFINITY) ? 0.f : ex2_approx(m1 - mm);
+                const float lsum = a0 * l + a1 * l1;
+                const float w0 = a0 * (o_scale / lsum), w1 = a1 * (o_scale / lsum);
+                const bool has1 = n_kv >= 2;  // warpgroup 1 had key blocks: O_1 holds them
+                const size_t orow = (static_cast<size_t>(I.bh) * N + qrow) * D;
+#pragma unroll
+                for (int q4 = 0; q4 < D / 32; ++q4) {
+                    uint32_t ov[32];
+                    tmem_ld32(lane_base + C::kColO0 + 32 * q4, ov);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * w0);
+                    if (has1) {
+                        uint32_t ow[32];
+                        tmem_ld32(lane_base + C::kColO1 + 32 * q4, ow);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            ov[e] = __float_as_uint(fmaf(__uint_as_float(ow[e]), w1, __uint_as_float(ov[e])));
+                    }
+                    if (qrow < N) {
+                        uint32_t w[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            w[e] = pack_bf16x2(__uint_as_float(ov[2 * e]), __uint_as_float(ov[2 * e + 1]));
+                        uint4* out = reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.o) + orow + 32 * q4);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            out[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(smem_u32(&bars.merge_done));
+                if (qrow < N && args.lse != nullptr)
+                    args.lse[static_cast<size_t>(I.bh) * N + qrow] = (mm + log2f(lsum)) * 0.69314718055994530942f;
+                continue;
+            }
             // A row that saw no key (l = 0; only in a causal key shard) gives O = 0 and
             // lse = -inf.  O_t is read before this warp publishes the next item's first P,
             // so the next item's first P V (which overwrites O_t) comes after these loads.
@@ -695,7 +827,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int q4 = 0; q4 < D / 32; ++q4) {
                 uint32_t ov[32];
-                if (!SHARD || n_kv > 0) {
+                if (i > 0) {
                     tmem_ld32(lane_base + colO + 32 * q4, ov);
                 } else {
 #pragma unroll
@@ -763,13 +895,6 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse
     a.delta = delta;
     a.n_pairs = (N + 2 * kBM - 1) / (2 * kBM);
     a.BH = BH;
-    {
-        // causal scheduling groups: as many heads as keep their K/V within ~64 MB of L2
-        // (K/V bytes per query head: a K/V head's K and V over the heads that share it)
-        const double kv_head = 2.0 * static_cast<double>(N_kv) * D * C::kElem / (H / H_kv);
-        long long g = static_cast<long long>(64.0 * 1024 * 1024 / (kv_head > 1.0 ? kv_head : 1.0));
-        a.hgrp = static_cast<int>(g < 1 ? 1 : (g > BH ? BH : g));
-    }
     a.c_log2 = c_log2;
     a.o_scale = o_scale;
     a.causal = causal;
@@ -785,8 +910,23 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse
     // 4-8% slower than letting the next CTA take the first free SM.
     int sms = 152;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int n_items = a.n_pairs * BH;
-    const int grid = (FP8 || n_items < sms) ? n_items : sms;
+    const int pairs = a.n_pairs * BH;
+    a.n_pair_items = pairs;
+    a.n_items = pairs;
+    int grid = pairs;
+    if (!FP8) {
+        // When the last round of pairs fills at most half the CTAs, its pairs are dealt as
+        // twice as many single tiles, all in that last round (bf16 forward, not shards).
+        // Causal items run heaviest first, so after a full round the last one holds the
+        // lightest pairs, whose split measured slower: there, only a single round is split.
+        const int rounds = (pairs + sms - 1) / sms;
+        const int last = pairs - (rounds - 1) * sms;
+        if (!SHARD && 2 * last <= sms && (!causal || rounds == 1)) {
+            a.n_pair_items = pairs - last;
+            a.n_items = pairs + last;
+        }
+        grid = rounds > 1 ? sms : a.n_items;
+    }
     return static_cast<int>(launch_pdl(fwd_sm103_kernel<D, FP8, SHARD, PB>, dim3(grid), dim3(kThreads),
                                        C::kSmemAlloc, s, tq, tk, tv, a));
 }

@@ -136,6 +136,53 @@ def test_bf16_many_heads_ragged_n_every_head(d, causal):
             assert max_err(lse_c[b, h, rows], lse_ref) <= TOL_LSE_BF16, f"batch {b} head {h}"
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_single_tile_items_between_pairs(d, causal):
+    # N = 300: each head has one whole tile pair and a last pair whose second tile lies
+    # past N, which runs as a single-tile item (its key blocks alternate between the two
+    # softmax warpgroups, whose halves are merged at the end).  400 items on the persistent
+    # CTAs, so each CTA works through pairs and single tiles in turn, and the two tiles'
+    # per-block barrier counts drift apart.  Whole tensors against the oracle.
+    B, H, N = 2, 100, 300
+    x, dev = device_inputs(B, H, N, d, "bf16")
+    s = scale_for(d)
+    o, lse = run_fwd(dev, fa.FA_BF16, s, causal)
+    o_ref, lse_ref = oracle.attn_fwd(f64(x["q"]), f64(x["k"]), f64(x["v"]), s, causal)
+    assert max_err(f64(o), o_ref) <= TOL_BF16_O
+    assert max_err(f64(lse), lse_ref) <= TOL_LSE_BF16
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_last_round_as_single_tiles(d, causal):
+    # 40 heads x 4 pairs = 160 pairs: one full round on 152 CTAs; without the causal mask the
+    # 8 pairs left for the second round are dealt as 16 single tiles (causal runs keep the
+    # pairs there).  Whole tensors against the oracle.
+    B, H, N = 1, 40, 1024
+    x, dev = device_inputs(B, H, N, d, "bf16")
+    s = scale_for(d)
+    o, lse = run_fwd(dev, fa.FA_BF16, s, causal)
+    o_ref, lse_ref = oracle.attn_fwd(f64(x["q"]), f64(x["k"]), f64(x["v"]), s, causal)
+    assert max_err(f64(o), o_ref) <= TOL_BF16_O
+    assert max_err(f64(lse), lse_ref) <= TOL_LSE_BF16
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_fewer_pairs_than_sms_run_as_single_tiles(d, causal):
+    # 4 heads x 16 pairs = 64 pairs, fewer than half the SMs: every pair is dealt as two
+    # single-tile items, and each warpgroup sweeps 16 of the 32 key blocks.  Whole tensors
+    # against the oracle.
+    B, H, N = 1, 4, 4096
+    x, dev = device_inputs(B, H, N, d, "bf16")
+    s = scale_for(d)
+    o, lse = run_fwd(dev, fa.FA_BF16, s, causal)
+    o_ref, lse_ref = oracle.attn_fwd(f64(x["q"]), f64(x["k"]), f64(x["v"]), s, causal)
+    assert max_err(f64(o), o_ref) <= TOL_BF16_O
+    assert max_err(f64(lse), lse_ref) <= TOL_LSE_BF16
+
+
 def test_bf16_deterministic_and_lse_optional():
     x, dev = device_inputs(1, 2, 700, 128, "bf16")
     s = scale_for(128)
