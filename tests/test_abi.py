@@ -105,13 +105,26 @@ def test_size_limits(L):
 
 
 def test_fp8_argument_errors(L):
-    def f(qd=1.0, d=128, N=128):
-        return L.fa_fwd_fp8(P, P, P, P, None, qd, 1.0, 1.0, 1, 1, N, d, 0.1, 0, None)
+    def f(qd=1.0, d=128, N=128, scale=0.1):
+        return L.fa_fwd_fp8(P, P, P, P, None, qd, 1.0, 1.0, 1, 1, N, d, scale, 0, None)
     assert f(qd=0.0) == 1
     assert f(qd=-1.0) == 1
     assert f(qd=float("inf")) == 1
+    assert f(qd=float("nan")) == 1
     assert f(N=0) == 1
+    assert f(scale=float("nan")) == 1
     assert f(d=64) == 2
+
+
+def test_gqa_forward_argument_errors(L):
+    def g(H=4, H_kv=2, d=64, dtype=1, scale=0.125):
+        return L.fa_fwd_gqa(P, P, P, P, None, 1, H, H_kv, 128, d, scale, 0, dtype, None)
+    assert g(H_kv=0) == 1
+    assert g(H_kv=3) == 1                # 4 % 3 != 0
+    assert g(scale=float("inf")) == 1
+    assert g(dtype=2) == 1               # E4M3 goes through the fp8 entry points
+    assert g(dtype=0) == 2               # fp32 inputs: not on this path
+    assert g(d=96) == 2
 
 
 @pytest.mark.parametrize("name", ["fa_fwd_fp8_per_head", "fa_fwd_fp8_per_block"])
@@ -139,6 +152,7 @@ def test_bwd_argument_errors(L):
     assert b(ws_bytes=ws - 4) == 1
     assert b(dtype=9) == 1
     assert b(dtype=0) == 2
+    assert b(dtype=2) == 2               # no E4M3 backward
     assert b(d=96) == 2
 
 
@@ -163,15 +177,20 @@ def test_kv_shard_argument_errors(L):
     assert f(H_kv=3) == 1
     assert f(dtype=0) == 2             # fp32 inputs: not on this path
     assert f(d=96) == 2
+    assert f(Nkv=(1 << 24) + 1) == 2   # keys per shard beyond 2^24
 
 
 def test_lse_merge_argument_errors(L):
-    def m(op=P, lp=P, o=P, S=2, d=64, dtype=1, lse=None):
-        return L.fa_lse_merge(op, lp, S, o, lse, 1, 1, 128, d, dtype, None)
+    def m(op=P, lp=P, o=P, S=2, d=64, dtype=1, lse=None, B=1, H=1, N=128):
+        return L.fa_lse_merge(op, lp, S, o, lse, B, H, N, d, dtype, None)
     assert m(op=None) == 1
     assert m(lp=MIS) == 1
     assert m(lse=MIS) == 1
     assert m(S=0) == 1
+    assert m(N=0) == 1
     assert m(dtype=2) == 1
     assert m(d=32) == 2
+    assert m(S=17) == 2                # at most 16 parts
+    # B*H*N rows times parts beyond 2^40 elements are refused, not wrapped
+    assert m(B=1 << 10, H=1 << 10, N=1 << 21) == 2
     assert m(S=17) == 2
